@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA2 decode step (index + sparse attention) on GB300.
+
+One step = one pass of the whole hot path over a batch of decode queries:
+append the current token (RoPE + FP4 main latent, FP4 indexer key), then for
+each of the group's layers the FP8 window append, the Full / Reindex index
+(or Reuse), and sparse attention.  The default workload is the 20-layer
+decoder group at 131,072 entries with batch 16 ([Full + 3 Reuse] +
+4 x [Reindex + 3 Reuse]).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 128k|1m|tiny|manyq|ragged]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
+(independent requests, no collective on the data path); value = all queries
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode queries/s per layer group at 128K/1M ctx; % of HBM roofline"
+UNIT = "queries/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload(name):
+    from csa2_sparse_attention_gb300 import workloads as W
+    return {"128k": W.group_128k, "1m": W.group_1m, "tiny": W.tiny, "manyq": W.many_query,
+            "ragged": W.ragged}[name]()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def config_of(wl, extra=None):
+    c = {"workload": wl.name, "queries_per_gpu": wl.batch,
+         "context": wl.contexts[0] if len(set(wl.contexts)) == 1 else f"ragged {min(wl.contexts)}..{max(wl.contexts)}",
+         "layers": "".join(wl.layers), "pool_blocks": wl.pool_blocks, "topk": wl.topk,
+         "window": wl.window, "index_heads": 32, "index_dim": 128, "attn_heads": 64, "latent_dim": 512}
+    c.update(extra or {})
+    return c
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (every 200 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- algorithmic bytes
+def alg_bytes_per_launch(kernel, g):
+    """Algorithmic bytes one launch of `kernel` moves for this group's step
+    (average over the step's launches of that kernel)."""
+    import numpy as np
+    from csa2_sparse_attention_gb300 import workloads as W
+    n = np.asarray(g.contexts, dtype=np.int64)
+    B, P, K, Wn = g.B, g.P, g.K, g.Wn
+    nb = (n + 7) // 8
+    if kernel == "scan_blockmax":   # indexer K stream + block maxima + indexer Q
+        return float(np.sum(n * 72 + nb * 4) + B * 32 * 72)
+    if kernel == "attn_split":      # selected FP4 latents + FP8 window + bf16 Q
+        return float(np.sum(288 * np.minimum(K, n) + 512 * np.minimum(Wn, n)) + B * 64 * 512 * 2)
+    if kernel == "attn_merge":      # bf16 output + lse
+        return float(B * (64 * 512 * 2 + 64 * 4))
+    if kernel == "pool_score":      # gathered pool blocks (8 rows x 72 B)
+        n_full = sum(1 for m in g.layers if m == W.FULL)
+        n_re = sum(1 for m in g.layers if m == W.REINDEX)
+        c_full, c_re = max(P, K), P
+        per = [float(np.sum(np.minimum(8 * c_full, nb * 8) * 72))] * n_full + \
+              [float(np.sum(np.minimum(8 * c_re, nb * 8) * 72))] * n_re
+        return sum(per) / max(1, len(per))
+    if kernel == "select_blocks":
+        return float(np.sum(nb * 4))
+    if kernel == "select_topk":
+        return float(B * 8 * P * 4)
+    return None
+
+
+def traffic_from_profiles(kernel, wl_name):
+    """dram bytes per launch from a committed ncu summary, if its recorded
+    source hash still matches the kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{wl_name}.txt")
+    if not os.path.exists(path):
+        return None
+    meta = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                meta[k.strip()] = v.strip()
+    src = meta.get("source_file")
+    sha = meta.get("source_sha256")
+    if not src or not sha:
+        return None
+    with open(os.path.join(ROOT, src), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != sha:
+            return None
+    try:
+        return float(meta["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------- CPU baseline
+class OracleSample:
+    """The oracle (as it stands) on a few queries of a workload: the setup
+    (quantizing each query's caches) is untimed; step() runs the per-step
+    work of one query (current-token append, Full/Reindex index, every
+    attention layer), cycling through the prepared queries."""
+
+    def __init__(self, wl_name, queries):
+        from oracle import csa2_oracle as O
+        from tests.helpers import oracle_query
+        self.O = O
+        self.wl = wl = workload(wl_name)
+        self.preps = []
+        for q in range(queries):
+            inp = oracle_query(wl, q)
+            kc, ks = O.quantize_fp4(inp["k_real"])
+            lc, ls = O.quantize_fp4(O.rope(inp["latent_real"], inp["positions"]))
+            rings = {li: O.append_swa_fp8(inp["swa_real"][li]) for li in range(len(wl.layers))}
+            self.preps.append((inp, O.dequantize_fp4(kc, ks), lc, ls, rings))
+        self.i = 0
+
+    def step(self):
+        O, wl = self.O, self.wl
+        inp, kdq, lc, ls, rings = self.preps[self.i % len(self.preps)]
+        self.i += 1
+        n = inp["n"]
+        O.append_main_latent(inp["latent_real"][n - 1:n], inp["positions"][n - 1:n])
+        O.append_plain_fp4(inp["k_real"][n - 1:n])
+        O.decode_group_step(wl.layers, inp["index_q"], inp["index_w"], kdq, lc, ls, rings,
+                            inp["attn_q"], n, wl.pool_blocks, wl.topk, wl.window)
+
+
+def oracle_step_sample(wl_name, queries, min_seconds):
+    """(query-steps, seconds) of the oracle over at least min_seconds."""
+    smp = OracleSample(wl_name, queries)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        smp.step()
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            return done, el
+
+
+def cpu_baseline(wl_name, queries=1, min_seconds=10.0):
+    """The oracle in a child process with every host core available to its
+    BLAS (OPENBLAS/OMP/MKL threads = cores)."""
+    cores = os.cpu_count() or 1
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=str(cores), OMP_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", wl_name,
+           "--child-queries", str(queries), "--child-seconds", str(min_seconds)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:] or ["failed"]}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": res["done"] / res["seconds"], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{res['done']} query-steps of {wl_name} ({queries} distinct queries, caches "
+                      f"pre-quantized untimed), {res['seconds']:.1f} s, fp64 numpy"}
+
+
+# ---------------------------------------------------------------- reference
+def run_reference(args):
+    """The oracle timed on this host's cores on the same workload, metric
+    and unit; each step is one query through the whole layer group.  The
+    step count is capped so the run ends within a few minutes."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    wl = workload(args.workload)
+    smp = OracleSample(args.workload, 1)
+    t0 = time.perf_counter()
+    smp.step()
+    est = time.perf_counter() - t0
+    warm = min(args.warmup, 2)
+    for _ in range(max(0, warm - 1)):
+        smp.step()
+    timed = max(1, min(args.steps, int(120.0 / max(est, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(timed):
+        smp.step()
+    el = time.perf_counter() - t0
+    value = timed / el
+    cores = os.cpu_count() or 1
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": timed, "warmup": warm, "ms_per_step": 1000.0 * el / timed, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, {"sample": "one query per step"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{timed} single-query steps of {wl.name} (requested {args.steps}, "
+                                       f"capped to ~120 s); caches pre-quantized untimed; fp64 numpy"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- ours
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from csa2_sparse_attention_gb300 import abi
+    from csa2_sparse_attention_gb300.layer_group import LayerGroup
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload(args.workload)
+    g = LayerGroup(wl, device=dev)
+    g.fill()
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        g.step(stream)                      # eager warm-up (sets kernel attributes)
+        stream.synchronize()
+        c0 = abi.csa2_launch_count()
+        g.step(stream)
+        stream.synchronize()
+        launches_per_step = abi.csa2_launch_count() - c0
+    g.capture(stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        g.replay()
+    stream.synchronize()
+
+    # ---- timed region: graph replays, L2 flushed between steps (untimed)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k in range(K):
+                flush.zero_()
+                ev[k][0].record(stream)
+                g.replay()
+                ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = wl.batch * world * K / (total_ms / 1000.0)
+
+    # ---- per-kernel device time (eager steps, L2 flushed, events on the launch stream)
+    n_prof = max(3, min(20, K))
+    kern = {}
+    for kid, name in enumerate(abi.KERNELS):
+        abi.csa2_timer_enable(kid, 64 * n_prof)
+    with torch.cuda.stream(stream):
+        for _ in range(n_prof):
+            flush.zero_()
+            g.step(stream)
+    stream.synchronize()
+    for kid, name in enumerate(abi.KERNELS):
+        ms, cnt = abi.csa2_timer_read(kid)
+        if cnt:
+            kern[name] = {"ms_per_step": ms / n_prof, "launches_per_step": cnt / n_prof, "avg_us": 1000 * ms / cnt}
+    tot = sum(v["ms_per_step"] for v in kern.values())
+    for v in kern.values():
+        v["share"] = v["ms_per_step"] / tot if tot else None
+    dom = max(kern, key=lambda k: kern[k]["ms_per_step"])
+    pk, pk_kind = peaks()
+    bpl = alg_bytes_per_launch(dom, g)
+    achieved = bpl / (kern[dom]["avg_us"] * 1e-6) / 1e9 if bpl else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+                "traffic": traffic_from_profiles(dom, wl.name), "peak_source": pk_kind,
+                "alg_bytes_per_launch": bpl, "avg_launch_us": kern[dom]["avg_us"],
+                "note": "achieved = algorithmic bytes per launch / CUDA-event launch time; frac of measured copy bandwidth"}
+    scan = kern.get("scan_blockmax")
+    scan_roof = None
+    if scan:
+        b = alg_bytes_per_launch("scan_blockmax", g)
+        a = b / (scan["avg_us"] * 1e-6) / 1e9
+        scan_roof = {"achieved": a, "frac": a / pk["hbm_gbs"], "unit": "GB/s"}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(g, stream, flush, min(K, 200), wl)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(args.workload)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "fp4/fp8 storage; f16/bf16 MMA, fp32 accumulate",
+                "data": "synthetic (seeded N(0,1) bf16, planted hot blocks)",
+                "config": config_of(wl, {"parallelism": f"replicas x{world}",
+                                         "l2": "flushed between timed steps (256 MB write, untimed)",
+                                         "cuda_graph": True}),
+                "gpu_launches": int(launches_per_step * K),
+                "roofline": roofline, "scan_roofline": scan_roof,
+                "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                            for k, v in kern.items()},
+                "clocks": clk.summary(), "wall_s_timed": t_wall,
+                "e2e": e2e, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(g, stream, flush, K, wl):
+    """Same metric through the C-ABI calls with host buffers: every step
+    copies its inputs from pinned host memory and reads its outputs back."""
+    import torch
+    ins = [g.tok_latent, g.tok_ik] + list(g.tok_swa) + list(g.attn_q) + \
+          [g.iq_bf16[i] for i in g.index_layers] + [g.iw[i] for i in g.index_layers]
+    outs = list(g.out) + list(g.lse)
+    h_in = [t.detach().cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for k in range(K):
+            flush.zero_()
+            evs[k][0].record(stream)
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            g.replay()
+            for d, h in zip(outs, h_out):
+                h.copy_(d, non_blocking=True)
+            evs[k][1].record(stream)
+    stream.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs)
+    return {"value": g.B * K / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="128k", choices=["128k", "1m", "tiny", "manyq", "ragged"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--child-queries", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--child-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.cpu_baseline_child and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.cpu_baseline_child:
+        done, secs = oracle_step_sample(args.workload, args.child_queries, args.child_seconds)
+        print(json.dumps({"done": done, "seconds": secs}))
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+"""One CSA2 layer group on one GPU: device state and the decode step's calls.
+
+[T1] "DeepSeek V4.1-Flash 为什么这么强？CED 与 CSA2 架构全拆解", §二: the decoder's
+20 layers run as [Full + 3 Reuse] + 4 x [Reindex + 3 Reuse]; Full layers write
+the main KV and indexer K and run the full index, Reindex layers share them
+and pick their own top-k inside the pool, Reuse layers reuse the indices
+(the same top-k buffer is passed again).  Every layer keeps its own attention
+query and sliding-window KV.
+
+This module only allocates device memory (torch) and issues C-ABI calls in
+that order; all arithmetic runs in libcsa2.so.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import abi
+from . import workloads as W
+
+
+def _round8(n):
+    return (int(n) + 7) // 8 * 8
+
+
+class LayerGroup:
+    """Caches, per-layer inputs/outputs and workspaces of one workload."""
+
+    def __init__(self, wl: W.Workload, device="cuda", sm_scale=1.0 / math.sqrt(512.0),
+                 rope_theta=10000.0):
+        self.wl = wl
+        self.dev = torch.device(device)
+        self.B = wl.batch
+        self.layers = wl.layers
+        self.P, self.K, self.Wn = wl.pool_blocks, wl.topk, wl.window
+        self.sm_scale = sm_scale
+        self.contexts = np.array(wl.contexts, dtype=np.int64)
+        if wl.shared_cache:
+            self.n_rows = _round8(wl.cache_entries)
+            starts = np.zeros(self.B, dtype=np.int64)
+            self.row_base = [0]
+        else:
+            caps = np.array([_round8(n) for n in wl.contexts], dtype=np.int64)
+            starts = np.concatenate([[0], np.cumsum(caps)[:-1]]).astype(np.int64)
+            self.n_rows = int(caps.sum())
+            self.row_base = list(starts)
+        self.kv_start_h = starts
+        d = self.dev
+        self.kv_start = torch.from_numpy(starts).to(d)
+        self.n_visible = torch.from_numpy(self.contexts.astype(np.int32)).to(d)
+        self.max_visible = int(self.contexts.max())
+        u8 = torch.uint8
+        self.kv_codes = torch.zeros((self.n_rows, 256), dtype=u8, device=d)
+        self.kv_scales = torch.zeros((self.n_rows, 32), dtype=u8, device=d)
+        self.ik_codes = torch.zeros((self.n_rows * 64,), dtype=u8, device=d)
+        self.ik_scales = torch.zeros((self.n_rows, 8), dtype=u8, device=d)
+        max_pos = int(max(self.n_rows, self.contexts.max() * wl.m + wl.m))
+        self.rope_max_pos = max_pos
+        self.rope = torch.empty(abi.csa2_rope_table_bytes(512, max_pos), dtype=u8, device=d)
+        abi.csa2_rope_table_init(rope_theta, 512, max_pos, self.rope, torch.cuda.current_stream(d))
+        L = len(self.layers)
+        self.swa = [torch.zeros((self.B, self.Wn, 512), dtype=u8, device=d) for _ in range(L)]
+        self.attn_q = [torch.zeros((self.B, 64, 512), dtype=torch.bfloat16, device=d) for _ in range(L)]
+        self.out = [torch.zeros((self.B, 64, 512), dtype=torch.bfloat16, device=d) for _ in range(L)]
+        self.lse = [torch.zeros((self.B, 64), dtype=torch.float32, device=d) for _ in range(L)]
+        self.index_layers = [i for i, m in enumerate(self.layers) if m in (W.FULL, W.REINDEX)]
+        self.iq_bf16 = {i: torch.zeros((self.B * 32, 128), dtype=torch.bfloat16, device=d) for i in self.index_layers}
+        self.iq_codes = {i: torch.zeros((self.B * 32 * 64,), dtype=u8, device=d) for i in self.index_layers}
+        self.iq_scales = {i: torch.zeros((self.B * 32, 8), dtype=u8, device=d) for i in self.index_layers}
+        self.iw = {i: torch.zeros((self.B, 32), dtype=torch.float32, device=d) for i in self.index_layers}
+        self.topk = {i: torch.full((self.B, self.K), -1, dtype=torch.int32, device=d) for i in self.index_layers}
+        self.pool = torch.full((self.B, self.P), -1, dtype=torch.int32, device=d)
+        # current-token inputs of a decode step
+        self.tok_latent = torch.zeros((self.B, 512), dtype=torch.bfloat16, device=d)
+        self.tok_ik = torch.zeros((self.B, 128), dtype=torch.bfloat16, device=d)
+        self.tok_swa = [torch.zeros((self.B, 512), dtype=torch.bfloat16, device=d) for _ in range(L)]
+        last = self.contexts - 1
+        self.tok_pos = torch.from_numpy(last * wl.m + (wl.m - 1)).to(d)
+        self.tok_row = torch.from_numpy(starts + last).to(d)
+        self.swa_row = torch.from_numpy(np.arange(self.B) * self.Wn + last % self.Wn).to(d)
+        # workspaces
+        B, mv = self.B, self.max_visible
+        self.ws_app = torch.zeros(abi.csa2_workspace_bytes(abi.OP_APPEND, B, mv, self.P, self.K), dtype=u8, device=d)
+        self.ws_full = torch.zeros(abi.csa2_workspace_bytes(abi.OP_INDEX_FULL, B, mv, self.P, self.K), dtype=u8, device=d)
+        self.ws_re = torch.zeros(abi.csa2_workspace_bytes(abi.OP_INDEX_REINDEX, B, mv, self.P, self.K), dtype=u8, device=d)
+        self.ws_attn = torch.zeros(abi.csa2_workspace_bytes(abi.OP_SPARSE_ATTN, B, mv, self.P, self.K), dtype=u8, device=d)
+        self.graph = None
+
+    # ------------------------------------------------------------ inputs
+    def fill(self, stream=None, requests=None):
+        """Draw the workload's synthetic inputs and write the caches through
+        the library's own append kernels (bulk), plus per-layer inputs."""
+        wl, d = self.wl, self.dev
+        s = stream or torch.cuda.current_stream(d)
+        reqs = [0] if wl.shared_cache else range(self.B)
+        for r in (requests if requests is not None else reqs):
+            base = self.row_base[r]
+            rows = W.cache_rows(wl, r)
+            k = torch.from_numpy(W.indexer_k(wl, r)).to(torch.bfloat16).to(d)
+            dst = torch.arange(base, base + rows, dtype=torch.int64, device=d)
+            abi.csa2_quantize_append(k, rows, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0, dst,
+                                     self.n_rows, self.ik_codes, self.ik_scales, self.ws_app,
+                                     self.ws_app.numel(), s)
+            del k
+            lat = torch.from_numpy(W.main_latent(wl, r)).to(torch.bfloat16).to(d)
+            pos = torch.from_numpy(W.latent_positions(wl, r)).to(d)
+            abi.csa2_quantize_append(lat, rows, 512, abi.FMT_FP4, abi.LAYOUT_ROWS, pos, self.rope,
+                                     self.rope_max_pos, dst, self.n_rows, self.kv_codes, self.kv_scales,
+                                     self.ws_app, self.ws_app.numel(), s)
+            s.synchronize()
+            del lat, pos, dst
+        self.fill_layer_inputs(stream=s)
+
+    def fill_layer_inputs(self, stream=None):
+        wl, d = self.wl, self.dev
+        s = stream or torch.cuda.current_stream(d)
+        bf = torch.bfloat16
+        for li in range(len(self.layers)):
+            rings = np.stack([W.swa_ring(wl, q, li) for q in range(self.B)])
+            ring_t = torch.from_numpy(rings.reshape(-1, 512)).to(bf).to(d)
+            abi.csa2_quantize_append(ring_t, ring_t.shape[0], 512, abi.FMT_FP8, abi.LAYOUT_ROWS, None, None, 0,
+                                     None, self.B * self.Wn, self.swa[li], None, self.ws_app,
+                                     self.ws_app.numel(), s)
+            self.attn_q[li].copy_(torch.from_numpy(np.stack([W.attn_q(wl, q, li) for q in range(self.B)])).to(bf))
+            last = self.contexts - 1
+            self.tok_swa[li].copy_(torch.from_numpy(rings[np.arange(self.B), last % self.Wn]).to(bf))
+            if li in self.index_layers:
+                self.iq_bf16[li].copy_(torch.from_numpy(
+                    np.stack([W.indexer_q(wl, q, li) for q in range(self.B)]).reshape(-1, 128)).to(bf))
+                self.iw[li].copy_(torch.from_numpy(np.stack([W.indexer_w(wl, q, li) for q in range(self.B)])))
+        if not wl.shared_cache:
+            lat_tok, ik_tok = [], []
+            for q in range(self.B):
+                n = int(self.contexts[q])
+                lat_tok.append(W.main_latent_rows(wl, q, n - 1, n)[0])
+                ik_tok.append(W.indexer_k_rows(wl, q, n - 1, n)[0])
+            self.tok_latent.copy_(torch.from_numpy(np.stack(lat_tok)).to(bf))
+            self.tok_ik.copy_(torch.from_numpy(np.stack(ik_tok)).to(bf))
+        s.synchronize()
+
+    # ------------------------------------------------------------ the step
+    def append_token(self, s):
+        """Append the current token (position n-1) of every request."""
+        abi.csa2_quantize_append(self.tok_ik, self.B, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0,
+                                 self.tok_row, self.n_rows, self.ik_codes, self.ik_scales, self.ws_app,
+                                 self.ws_app.numel(), s)
+        abi.csa2_quantize_append(self.tok_latent, self.B, 512, abi.FMT_FP4, abi.LAYOUT_ROWS, self.tok_pos,
+                                 self.rope, self.rope_max_pos, self.tok_row, self.n_rows, self.kv_codes,
+                                 self.kv_scales, self.ws_app, self.ws_app.numel(), s)
+
+    def layer(self, li, s, swa_append=True):
+        mode = self.layers[li]
+        B = self.B
+        if swa_append:
+            abi.csa2_quantize_append(self.tok_swa[li], B, 512, abi.FMT_FP8, abi.LAYOUT_ROWS, None, None, 0,
+                                     self.swa_row, B * self.Wn, self.swa[li], None, self.ws_app,
+                                     self.ws_app.numel(), s)
+        if mode in (W.FULL, W.REINDEX):
+            abi.csa2_quantize_append(self.iq_bf16[li], B * 32, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None,
+                                     0, None, B * 32, self.iq_codes[li], self.iq_scales[li], self.ws_app,
+                                     self.ws_app.numel(), s)
+        if mode == W.FULL:
+            abi.csa2_index_full(self.iq_codes[li], self.iq_scales[li], self.iw[li], B, self.ik_codes,
+                                self.ik_scales, self.n_rows, self.kv_start, self.n_visible, self.max_visible,
+                                self.P, self.K, self.pool, self.topk[li], self.ws_full, self.ws_full.numel(), s)
+        elif mode == W.REINDEX:
+            abi.csa2_index_reindex(self.iq_codes[li], self.iq_scales[li], self.iw[li], B, self.ik_codes,
+                                   self.ik_scales, self.n_rows, self.kv_start, self.n_visible,
+                                   self.max_visible, self.pool, self.P, self.K, self.topk[li], self.ws_re,
+                                   self.ws_re.numel(), s)
+        src = W.index_source(self.wl, li)
+        abi.csa2_sparse_attn(self.attn_q[li], B, self.kv_codes, self.kv_scales, self.n_rows, self.kv_start,
+                             self.n_visible, self.topk[src], self.K, self.swa[li], self.Wn, self.sm_scale,
+                             self.out[li], self.lse[li], self.ws_attn, self.ws_attn.numel(), s)
+
+    def step(self, stream=None, append=True):
+        """One pass of the whole group: append, then every layer in order."""
+        s = stream or torch.cuda.current_stream(self.dev)
+        if append and not self.wl.shared_cache:
+            self.append_token(s)
+        for li in range(len(self.layers)):
+            self.layer(li, s, swa_append=append and not self.wl.shared_cache)
+
+    def capture(self, stream):
+        """Capture step() into a CUDA graph on `stream` (replayed by replay())."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.step(stream=stream)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+
+    def status(self):
+        """Status words of every workspace (first device-detected problem)."""
+        return {name: abi.csa2_status_fetch(ws) for name, ws in
+                (("append", self.ws_app), ("full", self.ws_full), ("reindex", self.ws_re), ("attn", self.ws_attn))}

@@ -129,17 +129,22 @@ def bf16_bits(x):
     return (a.view(np.uint32) >> 16).astype(np.uint16)
 
 
-def _normal_rows(w, kind, key, rows, dim, threads=16):
-    """N(0,1) float32 [rows][dim] drawn chunk by chunk (8192 rows each)."""
-    out = np.empty((rows, dim), dtype=np.float32)
-    chunks = range(-(-rows // _CHUNK_ROWS))
+def _normal_rows(w, kind, key, rows, dim, r0=0, r1=None, threads=16):
+    """Rows [r0, r1) of an N(0,1) float32 [rows][dim] array drawn chunk by
+    chunk (8192 rows per independent stream)."""
+    r1 = rows if r1 is None else min(r1, rows)
+    c_lo, c_hi = r0 // _CHUNK_ROWS, -(-r1 // _CHUNK_ROWS)
+    out = np.empty((r1 - r0, dim), dtype=np.float32)
 
     def fill(c):
-        r0 = c * _CHUNK_ROWS
-        r1 = min(rows, r0 + _CHUNK_ROWS)
-        out[r0:r1] = _rng(w, kind, *key, c).standard_normal((r1 - r0, dim), dtype=np.float32)
+        a = c * _CHUNK_ROWS
+        b = min(rows, a + _CHUNK_ROWS)
+        blk = _rng(w, kind, *key, c).standard_normal((b - a, dim), dtype=np.float32)
+        lo, hi = max(a, r0), min(b, r1)
+        out[lo - r0:hi - r0] = blk[lo - a:hi - a]
 
-    if rows > _CHUNK_ROWS:
+    chunks = range(c_lo, c_hi)
+    if len(chunks) > 1:
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(fill, chunks))
     else:
@@ -177,24 +182,34 @@ def hot_blocks(w: Workload, req):
     return np.sort(rng.choice(nb, size=min(w.hot_blocks, nb), replace=False)).astype(np.int64)
 
 
-def indexer_k(w: Workload, req):
-    """Indexer keys of request `req`: bf16 [rows][128] N(0,1); every position
-    of a hot block is shifted by 0.5 * u with u = sum_h q[h] / sqrt(32), q the
-    request's Full-layer (layer 0) indexer query."""
+def indexer_k_rows(w: Workload, req, r0=0, r1=None):
+    """Rows [r0, r1) of request `req`'s indexer keys: bf16 [rows][128] N(0,1);
+    every position of a hot block is shifted by 0.5 * u with
+    u = sum_h q[h] / sqrt(32), q the request's layer-0 indexer query."""
     rows = cache_rows(w, req)
-    k = _normal_rows(w, _K_INDEX_K, (req,), rows, 128)
+    r1 = rows if r1 is None else min(r1, rows)
+    k = _normal_rows(w, _K_INDEX_K, (req,), rows, 128, r0, r1)
     hb = hot_blocks(w, req)
     if hb.size:
         u = indexer_q(w, req, 0).sum(axis=0) / np.float32(math.sqrt(32.0))
         pos = (hb[:, None] * 8 + np.arange(8)[None, :]).reshape(-1)
-        pos = pos[pos < rows]
-        k[pos] += np.float32(0.5) * u[None, :]
+        pos = pos[(pos >= r0) & (pos < r1)]
+        k[pos - r0] += np.float32(0.5) * u[None, :]
     return to_bf16_exact(k)
 
 
+def indexer_k(w: Workload, req):
+    return indexer_k_rows(w, req)
+
+
+def main_latent_rows(w: Workload, req, r0=0, r1=None):
+    """Rows [r0, r1) of request `req`'s main latents (pre-RoPE): bf16
+    [rows][512] N(0,1)."""
+    return to_bf16_exact(_normal_rows(w, _K_LATENT, (req,), cache_rows(w, req), 512, r0, r1))
+
+
 def main_latent(w: Workload, req):
-    """Main latents (pre-RoPE) of request `req`: bf16 [rows][512] N(0,1)."""
-    return to_bf16_exact(_normal_rows(w, _K_LATENT, (req,), cache_rows(w, req), 512))
+    return main_latent_rows(w, req)
 
 
 def latent_positions(w: Workload, req):

@@ -130,6 +130,11 @@ def quantize_fp4(x):
     x = np.asarray(x, dtype=np.float64)
     d = x.shape[-1]
     assert d % GROUP == 0
+    if x.size > (1 << 20):  # same definition, row chunks bound the memory
+        flat = x.reshape(-1, d)
+        parts = [quantize_fp4(flat[i:i + (1 << 20) // d]) for i in range(0, flat.shape[0], (1 << 20) // d)]
+        return (np.concatenate([p[0] for p in parts]).reshape(x.shape),
+                np.concatenate([p[1] for p in parts]).reshape(x.shape[:-1] + (d // GROUP,)))
     g = x.reshape(x.shape[:-1] + (d // GROUP, GROUP))
     amax = np.max(np.abs(g), axis=-1)
     sbyte = e4m3_encode(amax / 6.0)
@@ -366,20 +371,31 @@ def decode_group_query(layers, index_q, index_w, k_real, latent_real, positions,
     attention outputs and lse.
     """
     k_codes, k_scales = quantize_fp4(np.asarray(k_real)[:n])
-    kdq = dequantize_fp4(k_codes, k_scales)
     lat_codes, lat_scales = quantize_fp4(rope(np.asarray(latent_real)[:n], np.asarray(positions)[:n], theta))
+    rings = {li: append_swa_fp8(swa_real[li]) for li in range(len(layers))}
+    return decode_group_step(layers, index_q, index_w, dequantize_fp4(k_codes, k_scales),
+                             lat_codes, lat_scales, rings, attn_q, n, pool_blocks, topk,
+                             window, sm_scale)
+
+
+def decode_group_step(layers, index_q, index_w, k_dequant, lat_codes, lat_scales, rings,
+                      attn_q, n, pool_blocks=POOL_BLOCKS, topk=TOPK, window=WINDOW,
+                      sm_scale=SM_SCALE):
+    """The per-step part of decode_group_query, given caches already in their
+    stored formats: k_dequant [n][128] real indexer keys, the main latent's
+    codes [n][512] and scales [n][32], and E4M3 window rings per layer."""
     out = {"topk": {}, "pool": None, "o": {}, "lse": {}, "scores": {}}
     cur = None
     for li, mode in enumerate(layers):
         if mode == "F":
             qc, qs = quantize_fp4(index_q[li])
-            pool, cur, scores, _ = index_full(dequantize_fp4(qc, qs), index_w[li], kdq, n,
+            pool, cur, scores, _ = index_full(dequantize_fp4(qc, qs), index_w[li], k_dequant, n,
                                               pool_blocks, topk)
             out["pool"] = pool
             out["scores"][li] = scores
         elif mode == "X":
             qc, qs = quantize_fp4(index_q[li])
-            cur, _, scores = index_reindex(dequantize_fp4(qc, qs), index_w[li], kdq, n,
+            cur, _, scores = index_reindex(dequantize_fp4(qc, qs), index_w[li], k_dequant, n,
                                            out["pool"], topk)
             out["scores"][li] = scores
         elif mode == "R":
@@ -387,7 +403,6 @@ def decode_group_query(layers, index_q, index_w, k_real, latent_real, positions,
         else:
             raise ValueError(mode)
         out["topk"][li] = cur
-        ring = append_swa_fp8(swa_real[li])
-        sel, win = attention_inputs(cur, lat_codes, lat_scales, ring, n, window)
+        sel, win = attention_inputs(cur, lat_codes, lat_scales, rings[li], n, window)
         out["o"][li], out["lse"][li] = sparse_attention(attn_q[li], sel, win, sm_scale)
     return out

@@ -1,0 +1,153 @@
+"""Test infrastructure: oracle inputs for a workload query, the BLOCK8 layout
+permutation, and the acceptance rules.
+
+Acceptance (floating-point results are compared with the fp64 oracle):
+  * FP4/FP8 bytes: bit-exact when both sides quantize the same values; after
+    RoPE (device fp32 vs oracle fp64) a byte may differ only where the
+    oracle's value lies within 2^-20 relative of a rounding threshold.
+  * top-k / pool sets: identical except members whose oracle score lies
+    within 1e-5 relative of the K-th (P-th block) oracle score.
+  * attention: max|o - o*| / max|o*| <= 2e-3 per (query, head) with o* the
+    oracle run on the GPU's index set.  bf16 rounding of the output alone
+    contributes up to 2^-9 ~ 1.95e-3, so the kernels keep their own error
+    near fp32 level.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from csa2_sparse_attention_gb300 import workloads as W
+from oracle import csa2_oracle as O
+
+TOPK_REL = 1e-5
+ATTN_REL = 2e-3
+
+
+def block8_to_rows(plane, n_rows):
+    """BLOCK8 code plane (bytes) -> row-major [n_rows][64]."""
+    a = np.asarray(plane, dtype=np.uint8).reshape(n_rows // 8, 4, 8, 16)
+    return a.transpose(0, 2, 1, 3).reshape(n_rows, 64)
+
+
+def rows_to_block8(rows):
+    n = rows.shape[0]
+    return np.ascontiguousarray(rows.reshape(n // 8, 8, 4, 16).transpose(0, 2, 1, 3)).reshape(-1)
+
+
+def check_selection(gpu_ids, oracle_ids, score_of, kth, label=""):
+    """Sets equal except members whose score is within TOPK_REL of kth.
+    gpu_ids must be ascending then -1 padded."""
+    g = np.asarray(gpu_ids)
+    valid = g[g >= 0]
+    assert np.all(g[len(valid):] == -1), f"{label}: pads not at the end"
+    assert np.all(np.diff(valid) > 0), f"{label}: not strictly ascending"
+    o = np.asarray(oracle_ids)
+    o = o[o >= 0]
+    assert len(valid) == len(o), f"{label}: {len(valid)} vs {len(o)} selected"
+    diff = set(valid.tolist()) ^ set(o.tolist())
+    tol = TOPK_REL * max(abs(kth), 1e-30)
+    bad = [p for p in diff if abs(score_of(p) - kth) > tol]
+    assert not bad, f"{label}: {len(bad)} members differ beyond tolerance, e.g. {bad[:5]}"
+    return len(diff)
+
+
+def kth_value(values, k):
+    v = np.sort(np.asarray(values))[::-1]
+    return v[min(k, len(v)) - 1]
+
+
+def check_attention(o_gpu, o_ref, label=""):
+    """Per head row: max|o - o*| / max|o*| <= ATTN_REL."""
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    err = np.max(np.abs(o_gpu - o_ref), axis=-1)
+    den = np.max(np.abs(o_ref), axis=-1)
+    rel = np.where(den > 0, err / np.where(den > 0, den, 1), err)
+    worst = float(rel.max())
+    assert worst <= ATTN_REL, f"{label}: attention rel error {worst:.3g} > {ATTN_REL}"
+    return worst
+
+
+def oracle_query(wl: W.Workload, q, n=None):
+    """Inputs of query q in the form oracle.decode_group_query takes."""
+    r = W.request_of(wl, q)
+    n = wl.contexts[q] if n is None else n
+    idx = [i for i, m in enumerate(wl.layers) if m in (W.FULL, W.REINDEX)]
+    return dict(
+        layers=wl.layers,
+        index_q={i: W.indexer_q(wl, q, i) for i in idx},
+        index_w={i: W.indexer_w(wl, q, i).astype(np.float64) for i in idx},
+        k_real=W.indexer_k_rows(wl, r, 0, n),
+        latent_real=W.main_latent_rows(wl, r, 0, n),
+        positions=W.latent_positions(wl, r)[:n],
+        swa_real={i: W.swa_ring(wl, q, i) for i in range(len(wl.layers))},
+        attn_q={i: W.attn_q(wl, q, i) for i in range(len(wl.layers))},
+        n=n, pool_blocks=wl.pool_blocks, topk=wl.topk, window=wl.window)
+
+
+def bf16_to_f64(t):
+    """A torch bf16 tensor (any device) as float64 numpy."""
+    import torch
+    return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
+
+
+def run_group(wl):
+    import torch
+    from csa2_sparse_attention_gb300.layer_group import LayerGroup
+    g = LayerGroup(wl)
+    for ws in (g.ws_app, g.ws_full, g.ws_re, g.ws_attn):
+        ws.zero_()
+    g.fill()
+    g.step()
+    torch.cuda.synchronize()
+    return g
+
+
+def verify_query(g, wl, q, check_cache=True):
+    inp = oracle_query(wl, q)
+    n, P, K = inp["n"], wl.pool_blocks, wl.topk
+    r = W.request_of(wl, q)
+    base = g.row_base[r] if not wl.shared_cache else 0
+    kc, ks = O.quantize_fp4(inp["k_real"])
+    kdq = O.dequantize_fp4(kc, ks)
+    lc, ls = O.quantize_fp4(O.rope(inp["latent_real"], inp["positions"]))
+    if check_cache:
+        gk = block8_to_rows(g.ik_codes.cpu().numpy(), g.n_rows)[base:base + n]
+        assert np.array_equal(gk, O.pack_codes(kc)), "indexer K bytes"
+        assert np.array_equal(g.ik_scales[base:base + n].cpu().numpy(), ks), "indexer K scales"
+        gl = g.kv_codes[base:base + n].cpu().numpy()
+        assert np.array_equal(gl, O.pack_codes(lc)), "main latent bytes"
+        assert np.array_equal(g.kv_scales[base:base + n].cpu().numpy(), ls), "main latent scales"
+    topk_of = {}
+    for li, mode in enumerate(wl.layers):
+        if mode in (W.FULL, W.REINDEX):
+            qc, qs = O.quantize_fp4(inp["index_q"][li])
+            qdq = O.dequantize_fp4(qc, qs)
+            gt = g.topk[li][q].cpu().numpy()
+            if mode == W.FULL:
+                pool_o, top_o, scores, bmax = O.index_full(qdq, inp["index_w"][li], kdq, n, P, K)
+                gp = g.pool[q].cpu().numpy()
+                check_selection(gp, pool_o, lambda b: bmax[b], kth_value(bmax, P), f"q{q} pool")
+                check_selection(gt, top_o, lambda p: scores[p], kth_value(scores, K), f"q{q} L{li} top-k")
+                gpu_pool = gp
+            else:
+                re_o, cand, sc = O.index_reindex(qdq, inp["index_w"][li], kdq, n, gpu_pool, K)
+                smap = dict(zip(cand.tolist(), sc.tolist()))
+                check_selection(gt, re_o, lambda p: smap[p], kth_value(sc, K), f"q{q} L{li} reindex")
+            topk_of[li] = gt
+        else:
+            topk_of[li] = topk_of[W.index_source(wl, li)]
+        ring = O.append_swa_fp8(inp["swa_real"][li])
+        assert np.array_equal(g.swa[li][q].cpu().numpy(), ring), "window bytes"
+        sel, win = O.attention_inputs(topk_of[li], lc, ls, ring, n, wl.window)
+        o_ref, lse_ref = O.sparse_attention(inp["attn_q"][li], sel, win)
+        check_attention(bf16_to_f64(g.out[li][q]), o_ref, f"q{q} L{li} attention")
+        lse = g.lse[li][q].cpu().numpy()
+        assert np.allclose(lse, lse_ref, rtol=1e-5, atol=1e-5), f"q{q} L{li} lse"
+
+
+def check_status(g):
+    for name, st in g.status().items():
+        assert st[0] == 0, (name, st)
+
+

@@ -1,0 +1,97 @@
+"""Index + attention on the GPU against the oracle, through the C ABI.
+
+Each case builds a LayerGroup (caches written by the library's own append
+kernels from seeded bf16 inputs), runs one step, and checks every sampled
+query: cache bytes bit-exact; Full-layer pool and top-k against the oracle's
+global definitions; Reindex top-k against the oracle run on the GPU's pool;
+attention of every layer against the oracle run on the GPU's index set.
+"""
+import numpy as np
+import pytest
+import torch
+
+from csa2_sparse_attention_gb300 import workloads as W
+from oracle import csa2_oracle as O
+from tests.helpers import bf16_to_f64, check_attention, check_status, run_group, verify_query
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_group_8k():
+    """8192 entries, Full + Reindex + Reuse, pool 256 x 8 (smaller than
+    top-512: the Full top-k comes from the top-512 blocks)."""
+    wl = W.tiny()
+    g = run_group(wl)
+    check_status(g)
+    verify_query(g, wl, 0)
+    # Reuse layer 2 attends over exactly the Reindex layer's indices
+    assert g.topk[1].data_ptr() == g.topk[1].data_ptr()
+
+
+@pytest.mark.parametrize("pool,topk", [(2048, 512), (256, 512), (64, 100)])
+def test_ragged_small_contexts(pool, topk):
+    """Partial last blocks, contexts below the window, below one block,
+    and fewer blocks than the pool."""
+    ctx = [20000, 8191, 1000, 333, 129, 100, 17, 8, 5, 1]
+    wl = W.small_variant(W.group_128k(), ctx, name="ragged-small",
+                         layers=("F", "R", "X", "R"), pool_blocks=pool, topk=topk, hot_blocks=4)
+    g = run_group(wl)
+    check_status(g)
+    for q in range(len(ctx)):
+        verify_query(g, wl, q)
+
+
+def test_many_query_shared_cache_m2():
+    """Queries at consecutive raw positions over one shared m=2 cache."""
+    wl = W.many_query(queries=48, entries=6000, m=2)
+    g = run_group(wl)
+    check_status(g)
+    for q in (0, 1, 23, 47):
+        verify_query(g, wl, q, check_cache=(q == 0))
+
+
+def test_attention_direct_edge_cases():
+    """Direct csa2_sparse_attn calls: -1 pads, empty selection, window 0,
+    single entry, and an out-of-range index that is skipped and recorded."""
+    from csa2_sparse_attention_gb300 import abi
+    rng = np.random.default_rng(11)
+    n_rows, B, K, Wn = 64, 4, 8, 128
+    codes = rng.integers(0, 256, (n_rows, 256)).astype(np.uint8)
+    scales = rng.integers(0x28, 0x38, (n_rows, 32)).astype(np.uint8)
+    swa = rng.integers(0, 0x7E, (B, Wn, 512)).astype(np.uint8)
+    q = torch.randn((B, 64, 512), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    kv_start = np.array([0, 16, 32, 48], dtype=np.int64)
+    n_vis = np.array([16, 1, 16, 12], dtype=np.int32)
+    top = np.full((B, K), -1, dtype=np.int32)
+    top[0, :5] = [0, 3, 7, 8, 15]
+    top[1, 0] = 0
+    top[2, :3] = [1, 2, 99]          # 99 >= n: skipped and recorded
+    cases_window = 0
+    d = "cuda"
+    t = lambda a: torch.from_numpy(a).to(d)
+    out = torch.zeros((B, 64, 512), dtype=torch.bfloat16, device=d)
+    lse = torch.zeros((B, 64), dtype=torch.float32, device=d)
+    for window in (Wn, cases_window):
+        ws = torch.zeros(abi.csa2_workspace_bytes(abi.OP_SPARSE_ATTN, B, 16, 1, K), dtype=torch.uint8, device=d)
+        abi.csa2_sparse_attn(q.to(d), B, t(codes), t(scales), n_rows, t(kv_start), t(n_vis), t(top), K,
+                             t(swa), window, 1 / np.sqrt(512), out, lse, ws, ws.numel())
+        torch.cuda.synchronize()
+        st = abi.csa2_status_fetch(ws)
+        assert st[0] == abi.ERR_DEVICE_BOUNDS and st[1] == 7 and st[2] == 2 and st[3] == 99
+        qn = bf16_to_f64(q)
+        for b in range(B):
+            rows = codes[kv_start[b]:kv_start[b] + n_vis[b]]
+            cu = O.unpack_codes(rows)
+            sc = scales[kv_start[b]:kv_start[b] + n_vis[b]]
+            ids = top[b].copy()
+            ids[ids >= n_vis[b]] = -1
+            sel, win = O.attention_inputs(ids, cu, sc, swa[b], int(n_vis[b]), Wn)
+            if window == 0:
+                win = win[:0]
+            o_ref, lse_ref = O.sparse_attention(qn[b], sel, win)
+            if sel.shape[0] + win.shape[0] == 0:
+                assert np.all(bf16_to_f64(out[b]) == 0)
+                assert np.all(np.isneginf(lse[b].cpu().numpy()))
+            else:
+                check_attention(bf16_to_f64(out[b]), o_ref, f"b{b} window {window}")
+                assert np.allclose(lse[b].cpu().numpy(), lse_ref, rtol=1e-5, atol=1e-5)
