@@ -22,6 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_BOUNDS, 
 FMT_FP4, FMT_FP8 = 0, 1
 LAYOUT_ROWS, LAYOUT_BLOCK8 = 0, 1
 OP_APPEND, OP_INDEX_FULL, OP_INDEX_REINDEX, OP_SPARSE_ATTN = range(4)
+OUT_BF16, OUT_F32 = 0, 1
 INDEX_HEADS, INDEX_DIM, ATTN_HEADS, LATENT_DIM, BLOCK, STATUS_BYTES = 32, 128, 64, 512, 8, 256
 
 _p = ctypes.c_void_p
@@ -42,7 +43,7 @@ EXPORTS = {
     "csa2_index_full": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _int, _int, _p, _p, _p, _sz, _p]),
     "csa2_index_reindex": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p, _p, _sz, _p]),
     "csa2_sparse_attn": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _int, ctypes.c_float,
-                                _p, _p, _p, _sz, _p]),
+                                _p, _int, _p, _p, _sz, _p]),
     "csa2_launch_count": (_i64, []),
     "csa2_kernel_name": (ctypes.c_char_p, [_int]),
     "csa2_timer_enable": (_int, [_int, _int]),
@@ -137,11 +138,11 @@ def csa2_index_reindex(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_
 
 
 def csa2_sparse_attn(q_bf16, n_q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa,
-                     window, sm_scale, out_bf16, out_lse, ws, ws_bytes, stream=None):
+                     window, sm_scale, out, out_dtype, out_lse, ws, ws_bytes, stream=None):
     return _check("csa2_sparse_attn", lib.csa2_sparse_attn(
         _ptr(q_bf16), n_q, _ptr(kv_codes), _ptr(kv_scales), n_rows, _ptr(kv_start), _ptr(n_visible),
-        _ptr(topk), k, _ptr(swa), window, sm_scale, _ptr(out_bf16), _ptr(out_lse), _ptr(ws), ws_bytes,
-        _stream(stream)))
+        _ptr(topk), k, _ptr(swa), window, sm_scale, _ptr(out), out_dtype, _ptr(out_lse), _ptr(ws),
+        ws_bytes, _stream(stream)))
 
 
 KERNELS = ("scan_blockmax", "select_blocks", "pool_score", "select_topk", "attn_split",

@@ -67,9 +67,15 @@ extern "C" size_t csa2_workspace_bytes(int op, int64_t n_q, int32_t max_visible,
         case CSA2_OP_INDEX_REINDEX:
             if (pool_blocks < 1 || topk < 1) return 0;
             return reindex_ws(n_q, pool_blocks).total;
-        case CSA2_OP_SPARSE_ATTN:
+        case CSA2_OP_SPARSE_ATTN: {
             if (topk < 0) return 0;
-            return attn_ws(n_q, topk, kMaxWindow).total;
+            size_t m = 0;  // the split count depends on the window: take the largest
+            for (int win = 0; win <= kMaxWindow; ++win) {
+                const size_t t = attn_ws(n_q, topk, win).total;
+                m = t > m ? t : m;
+            }
+            return m;
+        }
         default: return 0;
     }
 }

@@ -29,7 +29,7 @@ class LayerGroup:
     """Caches, per-layer inputs/outputs and workspaces of one workload."""
 
     def __init__(self, wl: W.Workload, device="cuda", sm_scale=1.0 / math.sqrt(512.0),
-                 rope_theta=10000.0):
+                 rope_theta=10000.0, out_dtype=torch.float32):
         self.wl = wl
         self.dev = torch.device(device)
         self.B = wl.batch
@@ -63,7 +63,9 @@ class LayerGroup:
         L = len(self.layers)
         self.swa = [torch.zeros((self.B, self.Wn, 512), dtype=u8, device=d) for _ in range(L)]
         self.attn_q = [torch.zeros((self.B, 64, 512), dtype=torch.bfloat16, device=d) for _ in range(L)]
-        self.out = [torch.zeros((self.B, 64, 512), dtype=torch.bfloat16, device=d) for _ in range(L)]
+        self.out_dtype = out_dtype
+        self.out_code = abi.OUT_F32 if out_dtype == torch.float32 else abi.OUT_BF16
+        self.out = [torch.zeros((self.B, 64, 512), dtype=out_dtype, device=d) for _ in range(L)]
         self.lse = [torch.zeros((self.B, 64), dtype=torch.float32, device=d) for _ in range(L)]
         self.index_layers = [i for i, m in enumerate(self.layers) if m in (W.FULL, W.REINDEX)]
         self.iq_bf16 = {i: torch.zeros((self.B * 32, 128), dtype=torch.bfloat16, device=d) for i in self.index_layers}
@@ -173,7 +175,7 @@ class LayerGroup:
         src = W.index_source(self.wl, li)
         abi.csa2_sparse_attn(self.attn_q[li], B, self.kv_codes, self.kv_scales, self.n_rows, self.kv_start,
                              self.n_visible, self.topk[src], self.K, self.swa[li], self.Wn, self.sm_scale,
-                             self.out[li], self.lse[li], self.ws_attn, self.ws_attn.numel(), s)
+                             self.out[li], self.out_code, self.lse[li], self.ws_attn, self.ws_attn.numel(), s)
 
     def step(self, stream=None, append=True):
         """One pass of the whole group: append, then every layer in order."""

@@ -80,6 +80,9 @@ enum { CSA2_FMT_FP4 = 0, CSA2_FMT_FP8 = 1 };
  */
 enum { CSA2_LAYOUT_ROWS = 0, CSA2_LAYOUT_BLOCK8 = 1 };
 
+/* Output element type of csa2_sparse_attn. */
+enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
+
 /* Operation ids for csa2_workspace_bytes. */
 enum { CSA2_OP_APPEND = 0, CSA2_OP_INDEX_FULL = 1, CSA2_OP_INDEX_REINDEX = 2, CSA2_OP_SPARSE_ATTN = 3 };
 
@@ -206,8 +209,12 @@ csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t* q_scales, 
  *   topk     [n_q][k] int32 positions (a Full/Reindex layer's out_topk).
  *   swa      [n_q][window][512] E4M3 ring (slot = position mod window).
  *   window   0..128.
- *   out_bf16 [n_q][64][512] bf16; out_lse [n_q][64] fp32 natural-log
- *            log-sum-exp of the scaled logits, or NULL.
+ *   out      [n_q][64][512], bf16 (out_dtype CSA2_OUT_BF16) or fp32
+ *            (CSA2_OUT_F32); the result is rounded once, from fp32.  bf16's
+ *            unit roundoff is 2^-8, so the fp32 form carries the kernels'
+ *            own accuracy (about 1e-6 relative).
+ *   out_lse  [n_q][64] fp32 natural-log log-sum-exp of the scaled logits,
+ *            or NULL.
  * An empty E gives zeros and lse = -inf.  A topk entry outside [-1, n) is
  * skipped and recorded.
  */
@@ -215,7 +222,7 @@ csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q,
                              const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_rows,
                              const int64_t* kv_start, const int32_t* n_visible,
                              const int32_t* topk, int k, const uint8_t* swa, int window,
-                             float sm_scale, void* out_bf16, float* out_lse,
+                             float sm_scale, void* out, int out_dtype, float* out_lse,
                              void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /*

@@ -78,10 +78,13 @@ def test_host_argument_errors_return_before_launch(abi):
                                fake, fake, fake, 64, None)
     assert st == A.ERR_WORKSPACE
     st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, 129, 0.04,
-                                fake, None, fake, 1 << 30, None)
+                                fake, A.OUT_F32, None, fake, 1 << 30, None)
     assert st == A.ERR_INVALID_ARG  # window above 128
     st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, 128, -1.0,
-                                fake, None, fake, 1 << 30, None)
+                                fake, A.OUT_F32, None, fake, 1 << 30, None)
     assert st == A.ERR_INVALID_ARG
+    st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, 128, 0.04,
+                                fake, 7, None, fake, 1 << 30, None)
+    assert st == A.ERR_INVALID_ARG  # unknown output type
     with pytest.raises(A.Csa2Error):
         A.csa2_rope_table_init(10000.0, 512, 0, fake, None)

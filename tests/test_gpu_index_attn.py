@@ -69,12 +69,12 @@ def test_attention_direct_edge_cases():
     cases_window = 0
     d = "cuda"
     t = lambda a: torch.from_numpy(a).to(d)
-    out = torch.zeros((B, 64, 512), dtype=torch.bfloat16, device=d)
+    out = torch.zeros((B, 64, 512), dtype=torch.float32, device=d)
     lse = torch.zeros((B, 64), dtype=torch.float32, device=d)
     for window in (Wn, cases_window):
         ws = torch.zeros(abi.csa2_workspace_bytes(abi.OP_SPARSE_ATTN, B, 16, 1, K), dtype=torch.uint8, device=d)
         abi.csa2_sparse_attn(q.to(d), B, t(codes), t(scales), n_rows, t(kv_start), t(n_vis), t(top), K,
-                             t(swa), window, 1 / np.sqrt(512), out, lse, ws, ws.numel())
+                             t(swa), window, 1 / np.sqrt(512), out, abi.OUT_F32, lse, ws, ws.numel())
         torch.cuda.synchronize()
         st = abi.csa2_status_fetch(ws)
         assert st[0] == abi.ERR_DEVICE_BOUNDS and st[1] == 7 and st[2] == 2 and st[3] == 99
@@ -95,3 +95,25 @@ def test_attention_direct_edge_cases():
             else:
                 check_attention(bf16_to_f64(out[b]), o_ref, f"b{b} window {window}")
                 assert np.allclose(lse[b].cpu().numpy(), lse_ref, rtol=1e-5, atol=1e-5)
+
+
+def test_attention_bf16_output_within_its_rounding():
+    """The bf16 output is the fp32 result rounded once: within bf16's unit
+    roundoff (2^-8) of the oracle plus the fp32 path's own error."""
+    from csa2_sparse_attention_gb300.layer_group import LayerGroup
+    wl = W.tiny()
+    g = LayerGroup(wl, out_dtype=torch.bfloat16)
+    g.fill()
+    g.step()
+    torch.cuda.synchronize()
+    inp_check = verify_query.__globals__["oracle_query"](wl, 0)
+    from oracle import csa2_oracle as Orc
+    lc, ls = Orc.quantize_fp4(Orc.rope(inp_check["latent_real"], inp_check["positions"]))
+    for li in range(len(wl.layers)):
+        src = W.index_source(wl, li)
+        ring = Orc.append_swa_fp8(inp_check["swa_real"][li])
+        sel, win = Orc.attention_inputs(g.topk[src][0].cpu().numpy(), lc, ls, ring, wl.contexts[0], wl.window)
+        o_ref, _ = Orc.sparse_attention(inp_check["attn_q"][li], sel, win)
+        o = bf16_to_f64(g.out[li][0])
+        err = np.abs(o - o_ref)
+        assert np.all(err <= 2.0 ** -8 * np.abs(o_ref) + 1e-5 * np.abs(o_ref).max(axis=-1, keepdims=True))
