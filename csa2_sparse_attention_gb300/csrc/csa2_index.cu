@@ -20,6 +20,7 @@
 #include "csa2_common.cuh"
 #include "csa2_timer.cuh"
 #include "csa2_layout.cuh"
+#include "csa2_pipe.cuh"
 
 namespace csa2 {
 
@@ -154,55 +155,111 @@ __device__ __forceinline__ int32_t checked_visible(const int64_t* kv_start, cons
 }
 
 // ------------------------------------------------------------ full scan
-constexpr int kScanWarps = 8;
-constexpr int kScanChunk = 2048;  // positions per CTA
+// Producer/consumer pipeline.  One producer lane streams tiles of 128
+// positions (16 BLOCK8 blocks: 8 KB of codes, 1 KB of scales, each one
+// contiguous bulk copy) into a ring of kScanStages shared-memory stages;
+// eight consumer warps score 16 positions each per tile with the register
+// dequant + mma.sync core and write the block maxima.  CTA (x, q) scans a
+// contiguous range of query q's tiles.
+constexpr int kScanCW = 8;                       // consumer warps
+constexpr int kScanThreads = (kScanCW + 1) * 32;
+constexpr int kTile = 128;                       // positions per tile
+constexpr int kScanStages = 8;
 
-// grid (ceil(max_visible / 2048), n_q); block maxima of blocks [256x, 256x+256).
-__global__ void __launch_bounds__(kScanWarps * 32) scan_blockmax_kernel(
+struct ScanSmem {
+    uint8_t codes[kScanStages][kTile * 64];
+    uint8_t scales[kScanStages][kTile * 8];
+    uint64_t full[kScanStages];
+    uint64_t empty[kScanStages];
+};
+
+__global__ void __launch_bounds__(kScanThreads, 1) scan_blockmax_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales,
     const float* __restrict__ w, const uint8_t* __restrict__ k_codes,
     const uint8_t* __restrict__ k_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, float* __restrict__ blockmax,
-    int64_t nb_stride, Status* st) {
+    int64_t nb_stride, int ctas_per_query, Status* st) {
+    extern __shared__ __align__(128) uint8_t scan_smem_raw[];
+    ScanSmem& S = *reinterpret_cast<ScanSmem*>(scan_smem_raw);
     const int64_t q = blockIdx.y;
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, st,
                                       blockIdx.x == 0 && threadIdx.x == 0);
-    const int64_t base = int64_t(blockIdx.x) * kScanChunk;
-    if (base >= n) return;
+    const int64_t tiles_q = (int64_t(n) + kTile - 1) / kTile;
+    const int64_t per = (tiles_q + ctas_per_query - 1) / ctas_per_query;
+    const int64_t t0 = int64_t(blockIdx.x) * per;
+    const int64_t t1 = t0 + per < tiles_q ? t0 + per : tiles_q;
+    if (t0 >= t1) return;  // uniform over the CTA
     const int64_t ks = kv_start[q];
+    const int64_t nblk_vis = (int64_t(n) + 7) >> 3;
     const int lane = lane_id(), warp = threadIdx.x >> 5;
+    const int ntiles = int(t1 - t0);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kScanStages; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], kScanCW);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == kScanCW) {  // producer
+        if (lane == 0) {
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % kScanStages, r = i / kScanStages;
+                if (r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
+                    record(st, CSA2_ERR_TIMEOUT, 0, int32_t(q), i);
+                    break;
+                }
+                const int64_t t = t0 + i;
+                const int64_t nvb64 = nblk_vis - t * 16;
+                const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
+                mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
+                bulk_g2s(S.codes[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
+                bulk_g2s(S.scales[s], k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
+            }
+        }
+        return;
+    }
+
+    // consumers
     QFrag f;
     load_qfrag(f, q_codes, q_scales, w, q);
-    const int64_t end = base + kScanChunk < n ? base + kScanChunk : n;
-    const int64_t nblk_vis = (n + 7) >> 3;  // blocks holding visible positions
     float* out = blockmax + q * nb_stride;
-    KRaw cur, nxt;
-    int64_t p = base + 16 * warp;
-    auto fetch = [&](KRaw& k, int64_t p0) {
-        const int64_t b0 = p0 >> 3;
-        load_kraw(k, k_codes, k_scales, ks + p0 + (lane >> 2), b0 < nblk_vis,
-                  ks + p0 + 8 + (lane >> 2), b0 + 1 < nblk_vis);
-    };
-    if (p < end) fetch(cur, p);
-    for (; p < end; p += 16 * kScanWarps) {
-        const int64_t pn = p + 16 * kScanWarps;
-        if (pn < end) fetch(nxt, pn);
-        float s0, s1;
-        score_tile(f, cur, s0, s1);
-        const int64_t pos0 = p + (lane >> 2), pos1 = pos0 + 8;
-        float m0 = pos0 < n ? s0 : -INFINITY;
-        float m1 = pos1 < n ? s1 : -INFINITY;
+    const int tq = lane & 3, rr = lane >> 2;
+    for (int i = 0; i < ntiles; ++i) {
+        const int s = i % kScanStages, r = i / kScanStages;
+        if (!mbar_wait(&S.full[s], r & 1)) {
+            if (lane == 0) record(st, CSA2_ERR_TIMEOUT, 1, int32_t(q), i);
+            break;
+        }
+        const int64_t t = t0 + i;
+        const int64_t b0 = t * 16 + 2 * warp;  // first of this warp's two blocks
+        const bool v0 = b0 < nblk_vis, v1 = b0 + 1 < nblk_vis;
+        if (v0) {
+            KRaw k;
+            const uint8_t* cb = S.codes[s] + (2 * warp) * 512 + tq * 128 + rr * 16;
+            const uint8_t* sb = S.scales[s] + ((2 * warp) * 8 + rr) * 8 + 2 * tq;
+            k.c0 = *reinterpret_cast<const uint4*>(cb);
+            k.s0 = *reinterpret_cast<const uint16_t*>(sb);
+            k.c1 = v1 ? *reinterpret_cast<const uint4*>(cb + 512) : make_uint4(0, 0, 0, 0);
+            k.s1 = v1 ? *reinterpret_cast<const uint16_t*>(sb + 64) : 0u;
+            float s0, s1;
+            score_tile(f, k, s0, s1);
+            const int64_t pos0 = b0 * 8 + rr, pos1 = pos0 + 8;
+            float m0 = pos0 < n ? s0 : -INFINITY;
+            float m1 = pos1 < n ? s1 : -INFINITY;
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            for (int o = 4; o < 32; o <<= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            if (lane == 0) {
+                out[b0] = m0;
+                if (v1) out[b0 + 1] = m1;
+            }
         }
-        const int64_t b = p >> 3;
-        if (lane == 0) {
-            out[b] = m0;
-            if (b + 1 < nblk_vis) out[b + 1] = m1;
-        }
-        cur = nxt;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[s]);
     }
 }
 
@@ -259,147 +316,215 @@ __global__ void __launch_bounds__(kPoolWarps * 32) pool_score_kernel(
 }
 
 // ------------------------------------------------------------ selection
+// One 1024-thread CTA per query selects `count` of n keys (larger first,
+// ties to the lower index) and writes the selected indices in increasing
+// order.  Keys are uint32 images of the floats (float_key), staged in shared
+// memory when they fit.  An 8-bit radix pass over all keys picks the top
+// digit of the threshold; the keys sharing that digit are collected into a
+// short candidate list and the three remaining passes run on it.  The output
+// is compacted over warp-contiguous segments (coalesced reads, two block
+// scans) so it comes out in index order.
 constexpr int kSelThreads = 1024;
-constexpr int kSelSmemKeys = 16384;  // keys staged in shared memory (64 KB)
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelSmemKeys = 32768;  // keys staged in shared memory (128 KB)
+constexpr int kCandCap = 4096;       // candidates kept after the first pass
 
-// Block-wide exclusive scan of one int per thread; returns the block total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int& total, int* sh /*>= 33*/) {
-    const int lane = lane_id(), warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) sh[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int s = lane < nw ? sh[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
-        }
-        if (lane < nw) sh[lane] = s;  // inclusive warp prefix
-    }
-    __syncthreads();
-    total = sh[nw - 1];
-    const int before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
-    __syncthreads();
-    return before;
-}
+struct SelShared {
+    int hist[256];
+    int wsum[3][kSelWarps];
+    int misc[8];
+    uint32_t cand_key[kCandCap];
+};
 
 // Key of element i (float scores/maxima, larger first).
 struct KeySrc {
-    const float* g;   // global values
+    const float* g;     // global values
     const uint32_t* s;  // staged keys in shared memory, or null
     __device__ __forceinline__ uint32_t operator()(int i) const {
         return s ? s[i] : float_key(g[i]);
     }
 };
 
-// Threshold key T and how many keys equal to T to take so that exactly
-// `count` of the n keys are selected (keys > T plus the first ones == T in
-// index order).  8-bit radix passes, warp-aggregated histogram.
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Histogram of the 8-bit digit at `shift` of the keys produced by get(i) for
+// i < n that match (k & mask) == prefix; warp-aggregated with match_any.
+template <class Get>
+__device__ __forceinline__ void radix_hist(Get get, int n, uint32_t prefix, uint32_t mask, int shift,
+                                           int* hist) {
+    const int lane = lane_id();
+    for (int b = 0; b < n; b += blockDim.x) {
+        const int i = b + threadIdx.x;
+        bool m = false;
+        uint32_t d = 0;
+        if (i < n) {
+            const uint32_t k = get(i);
+            m = (k & mask) == prefix;
+            d = (k >> shift) & 0xFF;
+        }
+        const unsigned mm = __ballot_sync(0xffffffffu, m);
+        if (m) {
+            const unsigned peers = __match_any_sync(mm, d);
+            if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+        }
+    }
+}
+
+// Warp 0 finds the digit holding the `remaining`-th largest key; writes
+// misc[0] = digit, misc[1] = how many keys of that digit are still needed.
+__device__ __forceinline__ void radix_pick(const int* hist, int remaining, int* misc) {
+    const int lane = lane_id();
+    int c[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        sum += c[j];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int excl = incl - sum;
+    if (excl < remaining && remaining <= incl) {
+        int acc = excl, dsel = 255 - 8 * lane - 7;
+        for (int j = 0; j < 8; ++j) {
+            if (acc + c[j] >= remaining) {
+                dsel = 255 - 8 * lane - j;
+                break;
+            }
+            acc += c[j];
+        }
+        misc[0] = dsel;
+        misc[1] = remaining - acc;
+    }
+}
+
+// Threshold key T and the number of keys equal to T to take so that exactly
+// `count` (< n) keys are selected: keys > T plus the first keys == T.
 __device__ void radix_threshold(const KeySrc& key, int n, int count, uint32_t& thr, int& take_eq,
-                                int* hist /*[256]*/, int* sh) {
-    const int tid = threadIdx.x, lane = lane_id();
-    uint32_t prefix = 0, mask = 0;
-    int remaining = count;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
+                                SelShared& sm) {
+    const int tid = threadIdx.x;
+    for (int i = tid; i < 256; i += blockDim.x) sm.hist[i] = 0;
+    if (tid == 0) {
+        sm.misc[0] = 0;  // always a valid digit, even if no lane claims one
+        sm.misc[1] = 1;
+        sm.misc[2] = 0;
+    }
+    __syncthreads();
+    radix_hist(key, n, 0u, 0u, 24, sm.hist);
+    __syncthreads();
+    if (tid < 32) radix_pick(sm.hist, count, sm.misc);
+    __syncthreads();
+    uint32_t prefix = uint32_t(sm.misc[0]) << 24, mask = 0xFF000000u;
+    int remaining = sm.misc[1];
+    const int ncand = sm.hist[sm.misc[0]];
+    const bool use_cand = ncand <= kCandCap;
+    if (use_cand) {  // keys sharing the top digit
+        const int lane = lane_id();
         for (int b = 0; b < n; b += blockDim.x) {
             const int i = b + tid;
+            uint32_t k = 0;
             bool m = false;
-            uint32_t d = 0;
             if (i < n) {
-                const uint32_t k = key(i);
+                k = key(i);
                 m = (k & mask) == prefix;
-                d = (k >> shift) & 0xFF;
             }
             const unsigned mm = __ballot_sync(0xffffffffu, m);
-            if (m) {
-                const unsigned peers = __match_any_sync(mm, d);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
-            }
+            int base = 0;
+            if (lane == 0 && mm) base = atomicAdd(&sm.misc[2], __popc(mm));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (m) sm.cand_key[base + __popc(mm & lanemask_lt())] = k;
         }
+    }
+    __syncthreads();
+    for (int shift = 16; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += blockDim.x) sm.hist[i] = 0;
         __syncthreads();
-        if (tid < 32) {
-            // lane l owns bins 255-8l .. 248-8l (descending)
-            int c[8], sum = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[j] = hist[255 - 8 * lane - j];
-                sum += c[j];
-            }
-            int incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const int excl = incl - sum;  // keys in higher bins than this lane's
-            const bool here = excl < remaining && remaining <= incl;
-            if (here) {
-                int acc = excl, dsel = 255 - 8 * lane - 7;
-                for (int j = 0; j < 8; ++j) {
-                    if (acc + c[j] >= remaining) {
-                        dsel = 255 - 8 * lane - j;
-                        break;
-                    }
-                    acc += c[j];
-                }
-                sh[0] = dsel;
-                sh[1] = remaining - acc;
-            }
-        }
+        if (use_cand)
+            radix_hist([&](int i) { return sm.cand_key[i]; }, ncand, prefix, mask, shift, sm.hist);
+        else
+            radix_hist(key, n, prefix, mask, shift, sm.hist);
         __syncthreads();
-        prefix |= uint32_t(sh[0]) << shift;
+        if (tid < 32) radix_pick(sm.hist, remaining, sm.misc);
+        __syncthreads();
+        prefix |= uint32_t(sm.misc[0]) << shift;
         mask |= 0xFFu << shift;
-        remaining = sh[1];
+        remaining = sm.misc[1];
         __syncthreads();
     }
     thr = prefix;
     take_eq = remaining;
 }
 
-// Select `count` of n keys (see radix_threshold) and write out[j] = map(i) for
-// the selected i in increasing i; pads out[count..pad_to) with -1.
+// Select `count` of n keys and write out[j] = map(i) for the selected i in
+// increasing i; pads out[count..pad_to) with -1.
 template <class Map>
 __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, int32_t* out,
-                               Map map, int* hist, int* sh) {
-    const int tid = threadIdx.x;
+                               Map map, SelShared& sm) {
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
     if (count > n) count = n;
     if (count <= 0) {
         for (int i = tid; i < pad_to; i += blockDim.x) out[i] = -1;
         return;
     }
     uint32_t thr = 0;
-    int take_eq = 0;
-    if (count < n) {
-        radix_threshold(key, n, count, thr, take_eq, hist, sh);
-    } else {
-        thr = 0;  // every key is >= 0: take all keys equal to 0 too
-        take_eq = n;
-    }
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    int take_eq = n;  // count == n: every key (all are >= 0) is taken
+    if (count < n) radix_threshold(key, n, count, thr, take_eq, sm);
+    // warp-contiguous segments of whole 32-key chunks
+    const int seg = ((n + kSelWarps - 1) / kSelWarps + 31) & ~31;
+    const int lo = min(n, warp * seg), hi = min(n, lo + seg);
     int gt = 0, eq = 0;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t k = key(i);
-        gt += k > thr;
-        eq += k == thr;
+    for (int b = lo; b < hi; b += 32) {
+        const int i = b + lane;
+        const uint32_t k = i < hi ? key(i) : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, i < hi && k > thr));
+        eq += __popc(__ballot_sync(0xffffffffu, i < hi && k == thr));
     }
-    int tot;
-    const int eq_before = block_exclusive_scan(eq, tot, sh + 2);
-    int take = take_eq - eq_before;
-    take = take < 0 ? 0 : (take > eq ? eq : take);
-    const int out_before = block_exclusive_scan(gt + take, tot, sh + 2);
-    int o = out_before, e = 0;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t k = key(i);
-        if (k > thr || (k == thr && e++ < take)) out[o++] = map(i);
+    if (lane == 0) {
+        sm.wsum[0][warp] = gt;
+        sm.wsum[1][warp] = eq;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scans over warps: equal keys before, then selections before
+        const int e = sm.wsum[1][lane];
+        int ie = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, ie, o);
+            if (lane >= o) ie += y;
+        }
+        const int eq_before = ie - e;
+        int take = take_eq - eq_before;
+        take = take < 0 ? 0 : (take > e ? e : take);
+        const int sel = sm.wsum[0][lane] + take;
+        int is = sel;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, is, o);
+            if (lane >= o) is += y;
+        }
+        sm.wsum[1][lane] = eq_before;
+        sm.wsum[2][lane] = is - sel;
+    }
+    __syncthreads();
+    int eq_run = sm.wsum[1][warp], out_run = sm.wsum[2][warp];
+    for (int b = lo; b < hi; b += 32) {
+        const int i = b + lane;
+        const uint32_t k = i < hi ? key(i) : 0u;
+        const bool is_eq = i < hi && k == thr;
+        const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
+        const bool sel = (i < hi && k > thr) || (is_eq && eq_run + __popc(eqm & lanemask_lt()) < take_eq);
+        const unsigned sm_ = __ballot_sync(0xffffffffu, sel);
+        if (sel) out[out_run + __popc(sm_ & lanemask_lt())] = map(i);
+        eq_run += __popc(eqm);
+        out_run += __popc(sm_);
     }
     for (int i = count + tid; i < pad_to; i += blockDim.x) out[i] = -1;
 }
@@ -408,18 +533,18 @@ struct IdentityMap {
     __device__ __forceinline__ int32_t operator()(int i) const { return i; }
 };
 struct CandPosMap {
-    const int32_t* cand;
+    const int32_t* cand;  // shared-memory copy of the candidate blocks
     __device__ __forceinline__ int32_t operator()(int i) const { return 8 * cand[i >> 3] + (i & 7); }
 };
 
-// Top-`count` blocks by block maximum.  grid n_q, 1024 threads.
+// Top-`count` blocks by block maximum.  grid n_q, 1024 threads; dynamic
+// shared memory holds up to smem_keys_cap keys.
 __global__ void __launch_bounds__(kSelThreads) select_blocks_kernel(
     const float* __restrict__ blockmax, int64_t nb_stride, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, int64_t n_rows, int count,
     int32_t* __restrict__ out, int64_t out_stride, int smem_keys_cap) {
     extern __shared__ uint32_t smem_keys[];
-    __shared__ int hist[256];
-    __shared__ int sh[40];
+    __shared__ SelShared sm;
     const int64_t q = blockIdx.x;
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
     const int nb = (n + 7) >> 3;
@@ -430,39 +555,45 @@ __global__ void __launch_bounds__(kSelThreads) select_blocks_kernel(
         key.s = smem_keys;
         __syncthreads();
     }
-    select_compact(key, nb, count, count, out + q * out_stride, IdentityMap{}, hist, sh);
+    select_compact(key, nb, count, count, out + q * out_stride, IdentityMap{}, sm);
 }
 
-// Top-`count` positions among the scored candidates.  grid n_q, 1024 threads.
+// Top-`count` positions among the scored candidates.  grid n_q, 1024
+// threads; dynamic shared memory: C candidate blocks, then the keys.
 __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ cand,
     int64_t cand_stride, int C, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, int64_t n_rows, int count,
     int32_t* __restrict__ out, int64_t out_stride, int smem_keys_cap) {
-    extern __shared__ uint32_t smem_keys[];
-    __shared__ int hist[256];
-    __shared__ int sh[40];
+    extern __shared__ uint32_t smem_dyn[];
+    __shared__ SelShared sm;
+    int32_t* cblk = reinterpret_cast<int32_t*>(smem_dyn);
+    uint32_t* keys = smem_dyn + C;
     const int64_t q = blockIdx.x;
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
     const int32_t* cq = cand + q * cand_stride;
     const int nb = (n + 7) >> 3;
-    // positions that exist among the candidates
-    int valid = 0;
+    int valid = 0;  // positions that exist among the candidates
     for (int i = threadIdx.x; i < C; i += blockDim.x) {
         const int32_t b = cq[i];
+        cblk[i] = b;
         if (b >= 0 && b < nb) valid += min(8, n - 8 * b);
     }
-    int total;
-    block_exclusive_scan(valid, total, sh + 2);
+    for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, o);
+    if (lane_id() == 0) sm.wsum[0][threadIdx.x >> 5] = valid;
+    __syncthreads();
+    int total = 0;
+    for (int w = 0; w < kSelWarps; ++w) total += sm.wsum[0][w];
+    __syncthreads();
     const int m = 8 * C;
     const float* v = scores + q * score_stride;
     KeySrc key{v, nullptr};
     if (m <= smem_keys_cap) {
-        for (int i = threadIdx.x; i < m; i += blockDim.x) smem_keys[i] = float_key(v[i]);
-        key.s = smem_keys;
-        __syncthreads();
+        for (int i = threadIdx.x; i < m; i += blockDim.x) keys[i] = float_key(v[i]);
+        key.s = keys;
     }
-    select_compact(key, m, min(count, total), count, out + q * out_stride, CandPosMap{cq}, hist, sh);
+    __syncthreads();
+    select_compact(key, m, min(count, total), count, out + q * out_stride, CandPosMap{cblk}, sm);
 }
 
 // ------------------------------------------------------------ launches
@@ -486,14 +617,17 @@ static csa2_status check_index_args(const uint8_t* q_codes, const uint8_t* q_sca
 // Keys a selection launch stages in shared memory (all n, or none).
 static int sel_cap(int64_t n) { return n <= kSelSmemKeys ? int(n) : 0; }
 
-// Opt the selection kernels into 64 KB of dynamic shared memory, once per device.
+// Opt the selection kernels into their dynamic shared memory (keys plus, for
+// the top-k select, the candidate blocks), once per device.
 static csa2_status prepare_select_kernels() {
     static bool done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
     if (done[dev]) return CSA2_OK;
-    const int bytes = kSelSmemKeys * 4;
-    if (cudaFuncSetAttribute(select_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+    const int bytes = (kSelSmemKeys + kMaxPoolBlocks) * 4;
+    if (cudaFuncSetAttribute(scan_blockmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(ScanSmem))) != cudaSuccess ||
+        cudaFuncSetAttribute(select_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return CSA2_ERR_CUDA;
     done[dev] = true;
@@ -526,11 +660,15 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
     float* scores = reinterpret_cast<float*>(base + L.scores);
     const int C = pool_blocks > topk ? pool_blocks : topk;
     if (max_visible > 0) {
-        dim3 grid(unsigned(ceil_div<int64_t>(max_visible, kScanChunk)), unsigned(n_q));
+        // one CTA per SM: split each query's tiles over kSMs / n_q CTAs
+        const int64_t tiles_max = ceil_div<int64_t>(max_visible, kTile);
+        int64_t cpq = kSMs / n_q;
+        cpq = cpq < 1 ? 1 : (cpq > tiles_max ? tiles_max : cpq);
+        const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
         timer_begin(K_SCAN, s);
-        scan_blockmax_kernel<<<grid, kScanWarps * 32, 0, s>>>(q_codes, q_scales, w, k_codes, k_scales,
-                                                              n_rows, kv_start, n_visible, max_visible,
-                                                              blockmax, L.nb_stride, st);
+        scan_blockmax_kernel<<<grid, kScanThreads, sizeof(ScanSmem), s>>>(
+            q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, blockmax,
+            L.nb_stride, int(cpq), st);
         timer_end(K_SCAN, s);
     }
     const int cap_b = sel_cap(L.nb_stride);
@@ -560,7 +698,7 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
     timer_end(K_POOL_SCORE, s);
     const int cap_t = sel_cap(8 * int64_t(C));
     timer_begin(K_SELECT_TOPK, s);
-    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t) * 4, s>>>(
+    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + C) * 4, s>>>(
         scores, L.score_stride, cand, cand_stride, C, kv_start, n_visible, max_visible, n_rows, topk,
         out_topk, topk, cap_t);
     timer_end(K_SELECT_TOPK, s);
@@ -595,7 +733,7 @@ extern "C" csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t*
     timer_end(K_POOL_SCORE, s);
     const int cap_t = sel_cap(8 * int64_t(pool_blocks));
     timer_begin(K_SELECT_TOPK, s);
-    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t) * 4, s>>>(
+    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + pool_blocks) * 4, s>>>(
         scores, L.score_stride, pool, pool_blocks, pool_blocks, kv_start, n_visible, max_visible,
         n_rows, topk, out_topk, topk, cap_t);
     timer_end(K_SELECT_TOPK, s);
