@@ -42,7 +42,7 @@ EXPORTS = {
     "csa2_quantize_append": (_int, [_p, _i64, _int, _int, _int, _p, _p, _i64, _p, _i64, _p, _p, _p, _sz, _p]),
     "csa2_index_full": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _int, _int, _p, _p, _p, _sz, _p]),
     "csa2_index_reindex": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p, _p, _sz, _p]),
-    "csa2_sparse_attn": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _int, ctypes.c_float,
+    "csa2_sparse_attn": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _p, _int, ctypes.c_float,
                                 _p, _int, _p, _p, _sz, _p]),
     "csa2_launch_count": (_i64, []),
     "csa2_kernel_name": (ctypes.c_char_p, [_int]),
@@ -138,11 +138,11 @@ def csa2_index_reindex(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_
 
 
 def csa2_sparse_attn(q_bf16, n_q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa,
-                     window, sm_scale, out, out_dtype, out_lse, ws, ws_bytes, stream=None):
+                     swa_new_bf16, window, sm_scale, out, out_dtype, out_lse, ws, ws_bytes, stream=None):
     return _check("csa2_sparse_attn", lib.csa2_sparse_attn(
         _ptr(q_bf16), n_q, _ptr(kv_codes), _ptr(kv_scales), n_rows, _ptr(kv_start), _ptr(n_visible),
-        _ptr(topk), k, _ptr(swa), window, sm_scale, _ptr(out), out_dtype, _ptr(out_lse), _ptr(ws),
-        ws_bytes, _stream(stream)))
+        _ptr(topk), k, _ptr(swa), _ptr(swa_new_bf16), window, sm_scale, _ptr(out), out_dtype,
+        _ptr(out_lse), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 KERNELS = ("scan_blockmax", "select_blocks", "pool_score", "select_topk", "attn_split",

@@ -13,13 +13,23 @@
 // S = Q C^T (bf16 MMA, fp32 accumulate), the split's softmax statistics
 // (m, l), and O_s = P C with P split into f16 hi + lo parts (C converted in
 // place to f16, still exact), so the partial output carries ~2^-22 relative
-// error.  The merge kernel combines the splits with their log-sum-exp
-// weights and rounds once, to fp32 or bf16.
+// error.  When a query's splits fit one thread-block cluster (<= 8 CTAs) the
+// splits merge through distributed shared memory: each CTA keeps its partial
+// for half the dims at a time in its own shared memory and reduces one slice
+// of the dims over all peers.  Otherwise partials go to the workspace and a
+// merge kernel combines them.  Either way the result is rounded once, to
+// fp32 or bf16.
+//
+// Optionally the kernel also appends the current token's window latent: the
+// bf16 row for position n-1 is rounded to E4M3 (as csa2_quantize_append FP8
+// does), written to its ring slot, and used for that entry.
 #include "csa2_common.cuh"
 #include "csa2_timer.cuh"
 #include "csa2_layout.cuh"
 
 #include <cfloat>
+
+#include <cooperative_groups.h>
 
 namespace csa2 {
 
@@ -39,6 +49,8 @@ struct AttnSmem {
     uint32_t lut4[256];            // E2M1 pair -> bf16x2 (unscaled)
     uint16_t lut8[256];            // E4M3 byte -> bf16
     int ok[E];                     // entry valid
+    float ml[kH][2];               // this split's (m, l) per head
+    float wts[kH][16];             // merge weights a_s / L per head and split
 };
 
 // byte offset of 16-byte chunk c of row r in a [rows][512] 16-bit tile
@@ -90,13 +102,14 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
 
 // grid (splits, n_q), 256 threads.  Writes the split's unnormalized partial
 // O_s = sum_j exp(l_j - m_s) c_j (fp32 [64][512]) and (m_s, l_s) per head.
-template <int E>
+template <int E, bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(
     const uint16_t* __restrict__ qg, const uint8_t* __restrict__ kv_codes,
     const uint8_t* __restrict__ kv_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, const int32_t* __restrict__ topk, int k,
-    const uint8_t* __restrict__ swa, int window, float sm_scale,
-    float* __restrict__ part_o, float* __restrict__ part_ml, int splits, Status* st) {
+    uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, float sm_scale,
+    float* __restrict__ part_o, float* __restrict__ part_ml, int splits, void* __restrict__ out,
+    bool out_f32, float* __restrict__ out_lse, Status* st) {
     using Sm = AttnSmem<E>;
     constexpr int kSStride = Sm::kSStride, kPStride = Sm::kPStride;
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -182,10 +195,28 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(
             ok = true;
             const int64_t pos = int64_t(n - nw) + (ge - k);
             const int64_t slot = pos % window;
-            const uint4* src = reinterpret_cast<const uint4*>(swa + (q * window + slot) * kD + qq * 128);
+            uint8_t* ring = swa + (q * window + slot) * kD + qq * 128;
             uint4 v[8];
+            if (swa_new != nullptr && pos == n - 1) {
+                // current token: E4M3 of its bf16 latent, stored to the ring and used here
+                const uint4* src = reinterpret_cast<const uint4*>(swa_new + q * kD + qq * 128);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __ldg(src + j);
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 a = __ldg(src + 2 * j), b = __ldg(src + 2 * j + 1);
+                    const uint32_t w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        o4[m] = e4m3x2_rn_sat(bf16_lo(w8[2 * m]), bf16_hi(w8[2 * m])) |
+                                (e4m3x2_rn_sat(bf16_lo(w8[2 * m + 1]), bf16_hi(w8[2 * m + 1])) << 16);
+                    v[j] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                    reinterpret_cast<uint4*>(ring)[j] = v[j];
+                }
+            } else {
+                const uint4* src = reinterpret_cast<const uint4*>(ring);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = src[j];
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
@@ -282,9 +313,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
         if (c0 == 0) {
-            float* ml = part_ml + ((q * splits + split) * kH + h) * 2;
-            ml[0] = m;
-            ml[1] = l;
+            if (CLUSTER) {
+                S.ml[h][0] = m;
+                S.ml[h][1] = l;
+            } else {
+                float* ml = part_ml + ((q * splits + split) * kH + h) * 2;
+                ml[0] = m;
+                ml[1] = l;
+            }
         }
     }
     // C from bf16 to f16 in place (exact for FP4 and E4M3 values)
@@ -298,14 +334,16 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(
     }
     __syncthreads();
 
-    // O_s = P C: warp -> heads 16*hg.., dims 256*(warp/4).. in two passes of 128
+    // O_s = P C in two halves of 256 dims: warp -> heads 16*hg.., dims
+    // 256*half + 128*(warp/4) .. +128
     {
         const int dh = warp >> 2;
         const uint32_t ph = smem_addr(S.p_hi), pl = smem_addr(S.p_lo), cb = smem_addr(S.c);
         const int arow = 16 * hg + (lane & 7) + 8 * ((lane >> 3) & 1);
-        float* out = part_o + (q * splits + split) * int64_t(kH * kD);
-        for (int pass = 0; pass < 2; ++pass) {
-            const int d0 = 256 * dh + 128 * pass;  // first dim of this pass
+        float* part = part_o + (q * splits + split) * int64_t(kH * kD);
+        float* X = reinterpret_cast<float*>(S.q);  // [64][256] fp32 (Q is no longer needed)
+        for (int half = 0; half < 2; ++half) {
+            const int d0 = 256 * half + 128 * dh;  // first dim of this warp's slice
             float acc[16][4];
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
@@ -327,13 +365,62 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(
                 }
             }
             const int r = 16 * hg + (lane >> 2);
+            if (!CLUSTER) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c = d0 + 8 * j + 2 * (lane & 3);
+                    *reinterpret_cast<float2*>(part + r * kD + c) = make_float2(acc[j][0], acc[j][1]);
+                    *reinterpret_cast<float2*>(part + (r + 8) * kD + c) = make_float2(acc[j][2], acc[j][3]);
+                }
+                continue;
+            }
+            namespace cg = cooperative_groups;
+            cg::cluster_group cluster = cg::this_cluster();
+            if (half == 1) cluster.sync();  // peers finished reading the first half
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int c = d0 + 8 * j + 2 * (lane & 3);
-                *reinterpret_cast<float2*>(out + r * kD + c) = make_float2(acc[j][0], acc[j][1]);
-                *reinterpret_cast<float2*>(out + (r + 8) * kD + c) = make_float2(acc[j][2], acc[j][3]);
+                const int c = d0 - 256 * half + 8 * j + 2 * (lane & 3);
+                *reinterpret_cast<float2*>(X + r * 256 + c) = make_float2(acc[j][0], acc[j][1]);
+                *reinterpret_cast<float2*>(X + (r + 8) * 256 + c) = make_float2(acc[j][2], acc[j][3]);
+            }
+            cluster.sync();  // every partial of this half (and every (m, l)) is visible
+            const int rank = int(cluster.block_rank());
+            if (half == 0 && tid < kH) {
+                // merge weights of head tid over the splits
+                float M = -INFINITY;
+                for (int p = 0; p < splits; ++p) {
+                    const float* pml = cluster.map_shared_rank(&S.ml[0][0], p);
+                    M = fmaxf(M, pml[tid * 2]);
+                }
+                float L = 0.f, a[16];
+                for (int p = 0; p < splits; ++p) {
+                    const float* pml = cluster.map_shared_rank(&S.ml[0][0], p);
+                    const float mp = pml[tid * 2];
+                    a[p] = (M == -INFINITY || mp == -INFINITY) ? 0.f : expf(mp - M);
+                    L = fmaf(a[p], pml[tid * 2 + 1], L);
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                for (int p = 0; p < splits; ++p) S.wts[tid][p] = a[p] * inv;
+                if (rank == 0 && out_lse) out_lse[q * kH + tid] = L > 0.f ? M + logf(L) : -INFINITY;
+            }
+            __syncthreads();
+            // this CTA reduces dims [lo, hi) of the half over all peers
+            const int per = (256 + splits - 1) / splits;
+            const int lo = rank * per, hi = min(256, lo + per);
+            const int width = hi - lo;
+            for (int idx = tid; idx < kH * width; idx += kAttnThreads) {
+                const int h = idx / width, d = lo + idx % width;
+                float o = 0.f;
+                for (int p = 0; p < splits; ++p) {
+                    const float* px = cluster.map_shared_rank(X, p);
+                    o = fmaf(S.wts[h][p], px[h * 256 + d], o);
+                }
+                const int64_t oi = (q * kH + h) * int64_t(kD) + 256 * half + d;
+                if (out_f32) static_cast<float*>(out)[oi] = o;
+                else static_cast<uint16_t*>(out)[oi] = bf16_bits(o);
             }
         }
+        if (CLUSTER) cooperative_groups::this_cluster().sync();  // peers done with our shared memory
     }
 }
 
@@ -422,27 +509,42 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     if (lse && lane == 0) lse[q * kH + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
-template <int E>
+template <int E, bool CLUSTER>
 static csa2_status launch_split(dim3 grid, cudaStream_t s, const uint16_t* q, const uint8_t* kv_codes,
                                 const uint8_t* kv_scales, int64_t n_rows, const int64_t* kv_start,
-                                const int32_t* n_visible, const int32_t* topk, int k, const uint8_t* swa,
-                                int window, float sm_scale, float* part_o, float* part_ml, int splits,
+                                const int32_t* n_visible, const int32_t* topk, int k, uint8_t* swa,
+                                const uint16_t* swa_new, int window, float sm_scale, float* part_o,
+                                float* part_ml, int splits, void* out, bool out_f32, float* out_lse,
                                 Status* st) {
     static bool done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
     if (!done[dev]) {
-        if (cudaFuncSetAttribute(attn_split_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attn_split_kernel<E, CLUSTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnSmem<E>))) != cudaSuccess)
             return CSA2_ERR_CUDA;
         done[dev] = true;
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(AttnSmem<E>);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (CLUSTER) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = grid.x;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     timer_begin(K_ATTN_SPLIT, s);
-    attn_split_kernel<E><<<grid, kAttnThreads, sizeof(AttnSmem<E>), s>>>(
-        q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, window, sm_scale, part_o,
-        part_ml, splits, st);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_split_kernel<E, CLUSTER>, q, kv_codes, kv_scales, n_rows,
+                                             kv_start, n_visible, topk, k, swa, swa_new, window, sm_scale,
+                                             part_o, part_ml, splits, out, out_f32, out_lse, st);
     timer_end(K_ATTN_SPLIT, s);
-    return CSA2_OK;
+    return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
 }  // namespace csa2
@@ -452,9 +554,10 @@ using namespace csa2;
 extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* kv_codes,
                                         const uint8_t* kv_scales, int64_t n_rows,
                                         const int64_t* kv_start, const int32_t* n_visible,
-                                        const int32_t* topk, int k, const uint8_t* swa, int window,
-                                        float sm_scale, void* out, int out_dtype, float* out_lse,
-                                        void* ws, size_t ws_bytes, csa2_stream_t stream) {
+                                        const int32_t* topk, int k, uint8_t* swa,
+                                        const void* swa_new_bf16, int window, float sm_scale, void* out,
+                                        int out_dtype, float* out_lse, void* ws, size_t ws_bytes,
+                                        csa2_stream_t stream) {
     if (n_q < 0 || n_rows < 0 || k < 0 || k > kMaxTopk || window < 0 || window > kMaxWindow)
         return CSA2_ERR_INVALID_ARG;
     if (!(sm_scale > 0.f) || !(sm_scale < FLT_MAX)) return CSA2_ERR_INVALID_ARG;
@@ -462,6 +565,7 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     if (!q_bf16 || !kv_codes || !kv_scales || !kv_start || !n_visible || !out) return CSA2_ERR_INVALID_ARG;
     if (k > 0 && !topk) return CSA2_ERR_INVALID_ARG;
     if (window > 0 && !swa) return CSA2_ERR_INVALID_ARG;
+    if (swa_new_bf16 && (window == 0 || !aligned16(swa_new_bf16))) return CSA2_ERR_INVALID_ARG;
     if (!aligned16(q_bf16) || !aligned16(kv_codes) || !aligned16(out) || (swa && !aligned16(swa)))
         return CSA2_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(kv_scales) & 7) return CSA2_ERR_INVALID_ARG;
@@ -475,22 +579,33 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     float* part_o = reinterpret_cast<float*>(base + L.part_o);
     float* part_ml = reinterpret_cast<float*>(base + L.part_ml);
     const uint16_t* q = static_cast<const uint16_t*>(q_bf16);
-    dim3 grid(unsigned(L.splits), unsigned(n_q));
+    const uint16_t* sn = static_cast<const uint16_t*>(swa_new_bf16);
+    const bool f32 = out_dtype == CSA2_OUT_F32;
+    const bool cluster = L.splits <= 8;  // portable cluster size: merge through shared memory
+    const dim3 grid(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q));
     csa2_status e = CSA2_OK;
-#define CSA2_SPLIT(E_)                                                                             \
-    e = launch_split<E_>(grid, s, q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, \
-                         window, sm_scale, part_o, part_ml, L.splits, st)
-    switch (L.entries) {
-        case 80: CSA2_SPLIT(80); break;
-        case 64: CSA2_SPLIT(64); break;
-        case 48: CSA2_SPLIT(48); break;
-        case 32: CSA2_SPLIT(32); break;
-        default: CSA2_SPLIT(16); break;
+#define CSA2_SPLIT(E_, C_)                                                                              \
+    e = launch_split<E_, C_>(grid, s, q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, \
+                             sn, window, sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st)
+#define CSA2_SPLIT_E(C_)                      \
+    switch (L.entries) {                      \
+        case 80: CSA2_SPLIT(80, C_); break;   \
+        case 64: CSA2_SPLIT(64, C_); break;   \
+        case 48: CSA2_SPLIT(48, C_); break;   \
+        case 32: CSA2_SPLIT(32, C_); break;   \
+        default: CSA2_SPLIT(16, C_); break;   \
     }
+    if (cluster) {
+        CSA2_SPLIT_E(true)
+    } else {
+        CSA2_SPLIT_E(false)
+    }
+#undef CSA2_SPLIT_E
 #undef CSA2_SPLIT
     if (e != CSA2_OK) return e;
+    if (cluster) return launch_status();
     timer_begin(K_ATTN_MERGE, s);
-    if (out_dtype == CSA2_OUT_F32)
+    if (f32)
         attn_merge_kernel<true><<<dim3(unsigned(n_q), kH / 8), 256, 0, s>>>(part_o, part_ml, L.splits, out, out_lse);
     else
         attn_merge_kernel<false><<<dim3(unsigned(n_q), kH / 8), 256, 0, s>>>(part_o, part_ml, L.splits, out, out_lse);

@@ -332,7 +332,7 @@ constexpr int kCandCap = 4096;       // candidates kept after the first pass
 struct SelShared {
     int hist[256];
     int wsum[3][kSelWarps];
-    int misc[8];
+    int misc[kSelWarps];
     uint32_t cand_key[kCandCap];
 };
 
@@ -462,6 +462,62 @@ __device__ void radix_threshold(const KeySrc& key, int n, int count, uint32_t& t
     take_eq = remaining;
 }
 
+// Block-wide sum over the 1024 threads; every thread gets the total.
+__device__ __forceinline__ int block_sum(int v, int* red) {
+    const int lane = lane_id(), warp = threadIdx.x >> 5;
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int t = __reduce_add_sync(0xffffffffu, lane < int(blockDim.x >> 5) ? red[lane] : 0);
+    __syncthreads();
+    return t;
+}
+
+// Threshold by binary search over the key range with the keys held in
+// registers (KPT per thread, n <= KPT * 1024): the largest T with
+// count(key >= T) >= count, then take_eq = count - count(key > T).
+// At most 32 steps of KPT compares and one block sum each.
+template <int KPT>
+__device__ void bsearch_threshold(const uint32_t* keys, int n, int count, uint32_t& thr, int& take_eq,
+                                  SelShared& sm) {
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    uint32_t k[KPT];
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int i = tid + j * kSelThreads;
+        k[j] = i < n ? keys[i] : 0u;  // 0 sorts below every real key
+        if (i < n) {
+            kmin = min(kmin, k[j]);
+            kmax = max(kmax, k[j]);
+        }
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if (lane == 0) {
+        sm.wsum[0][warp] = int(kmin ^ 0x80000000u);
+        sm.wsum[1][warp] = int(kmax ^ 0x80000000u);
+    }
+    __syncthreads();
+    uint32_t lo = uint32_t(__reduce_min_sync(0xffffffffu, sm.wsum[0][lane])) ^ 0x80000000u;
+    uint32_t hi = uint32_t(__reduce_max_sync(0xffffffffu, sm.wsum[1][lane])) ^ 0x80000000u;
+    __syncthreads();
+    while (lo < hi) {
+        const uint32_t mid = lo + uint32_t((uint64_t(hi) - lo + 1) >> 1);
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) c += k[j] >= mid;
+        if (block_sum(c, sm.misc) >= count) lo = mid;
+        else hi = mid - 1;
+    }
+    int gt = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) gt += k[j] > lo;
+    gt = block_sum(gt, sm.misc);
+    thr = lo;
+    take_eq = count - gt;
+}
+
 // Select `count` of n keys and write out[j] = map(i) for the selected i in
 // increasing i; pads out[count..pad_to) with -1.
 template <class Map>
@@ -475,7 +531,16 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
     }
     uint32_t thr = 0;
     int take_eq = n;  // count == n: every key (all are >= 0) is taken
-    if (count < n) radix_threshold(key, n, count, thr, take_eq, sm);
+    if (count < n) {
+        if (key.s && n <= 8 * kSelThreads)
+            bsearch_threshold<8>(key.s, n, count, thr, take_eq, sm);
+        else if (key.s && n <= 16 * kSelThreads)
+            bsearch_threshold<16>(key.s, n, count, thr, take_eq, sm);
+        else if (key.s && n <= 32 * kSelThreads)
+            bsearch_threshold<32>(key.s, n, count, thr, take_eq, sm);
+        else
+            radix_threshold(key, n, count, thr, take_eq, sm);
+    }
     // warp-contiguous segments of whole 32-key chunks
     const int seg = ((n + kSelWarps - 1) / kSelWarps + 31) & ~31;
     const int lo = min(n, warp * seg), hi = min(n, lo + seg);

@@ -81,7 +81,6 @@ class LayerGroup:
         last = self.contexts - 1
         self.tok_pos = torch.from_numpy(last * wl.m + (wl.m - 1)).to(d)
         self.tok_row = torch.from_numpy(starts + last).to(d)
-        self.swa_row = torch.from_numpy(np.arange(self.B) * self.Wn + last % self.Wn).to(d)
         # workspaces
         B, mv = self.B, self.max_visible
         self.ws_app = torch.zeros(abi.csa2_workspace_bytes(abi.OP_APPEND, B, mv, self.P, self.K), dtype=u8, device=d)
@@ -153,12 +152,10 @@ class LayerGroup:
                                  self.kv_scales, self.ws_app, self.ws_app.numel(), s)
 
     def layer(self, li, s, swa_append=True):
+        """One layer: index (Full / Reindex; Reuse makes no call), then
+        attention with this layer's window append fused in (swa_append)."""
         mode = self.layers[li]
         B = self.B
-        if swa_append:
-            abi.csa2_quantize_append(self.tok_swa[li], B, 512, abi.FMT_FP8, abi.LAYOUT_ROWS, None, None, 0,
-                                     self.swa_row, B * self.Wn, self.swa[li], None, self.ws_app,
-                                     self.ws_app.numel(), s)
         if mode in (W.FULL, W.REINDEX):
             abi.csa2_quantize_append(self.iq_bf16[li], B * 32, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None,
                                      0, None, B * 32, self.iq_codes[li], self.iq_scales[li], self.ws_app,
@@ -174,7 +171,8 @@ class LayerGroup:
                                    self.ws_re.numel(), s)
         src = W.index_source(self.wl, li)
         abi.csa2_sparse_attn(self.attn_q[li], B, self.kv_codes, self.kv_scales, self.n_rows, self.kv_start,
-                             self.n_visible, self.topk[src], self.K, self.swa[li], self.Wn, self.sm_scale,
+                             self.n_visible, self.topk[src], self.K, self.swa[li],
+                             self.tok_swa[li] if swa_append else None, self.Wn, self.sm_scale,
                              self.out[li], self.out_code, self.lse[li], self.ws_attn, self.ws_attn.numel(), s)
 
     def step(self, stream=None, append=True):

@@ -208,6 +208,11 @@ csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t* q_scales, 
  *   kv_codes [n_rows][256], kv_scales [n_rows][32]: main latent, ROWS layout.
  *   topk     [n_q][k] int32 positions (a Full/Reindex layer's out_topk).
  *   swa      [n_q][window][512] E4M3 ring (slot = position mod window).
+ *   swa_new_bf16  [n_q][512] bf16 window latent of each query's current
+ *            token (position n-1), or NULL.  When given, the kernel rounds it
+ *            to E4M3 exactly as csa2_quantize_append (CSA2_FMT_FP8) would,
+ *            stores it to ring slot (n-1) mod window and uses it: the
+ *            window append fused into the attention call.
  *   window   0..128.
  *   out      [n_q][64][512], bf16 (out_dtype CSA2_OUT_BF16) or fp32
  *            (CSA2_OUT_F32); the result is rounded once, from fp32.  bf16's
@@ -221,8 +226,8 @@ csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t* q_scales, 
 csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q,
                              const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_rows,
                              const int64_t* kv_start, const int32_t* n_visible,
-                             const int32_t* topk, int k, const uint8_t* swa, int window,
-                             float sm_scale, void* out, int out_dtype, float* out_lse,
+                             const int32_t* topk, int k, uint8_t* swa, const void* swa_new_bf16,
+                             int window, float sm_scale, void* out, int out_dtype, float* out_lse,
                              void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /*

@@ -77,13 +77,13 @@ def test_host_argument_errors_return_before_launch(abi):
     st = A.lib.csa2_index_full(fake, fake, fake, 1, fake, fake, 16, fake, fake, 100, 2048, 512,
                                fake, fake, fake, 64, None)
     assert st == A.ERR_WORKSPACE
-    st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, 129, 0.04,
+    st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, None, 129, 0.04,
                                 fake, A.OUT_F32, None, fake, 1 << 30, None)
     assert st == A.ERR_INVALID_ARG  # window above 128
-    st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, 128, -1.0,
+    st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, None, 128, -1.0,
                                 fake, A.OUT_F32, None, fake, 1 << 30, None)
     assert st == A.ERR_INVALID_ARG
-    st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, 128, 0.04,
+    st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, None, 128, 0.04,
                                 fake, 7, None, fake, 1 << 30, None)
     assert st == A.ERR_INVALID_ARG  # unknown output type
     with pytest.raises(A.Csa2Error):

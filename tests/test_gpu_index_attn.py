@@ -74,7 +74,7 @@ def test_attention_direct_edge_cases():
     for window in (Wn, cases_window):
         ws = torch.zeros(abi.csa2_workspace_bytes(abi.OP_SPARSE_ATTN, B, 16, 1, K), dtype=torch.uint8, device=d)
         abi.csa2_sparse_attn(q.to(d), B, t(codes), t(scales), n_rows, t(kv_start), t(n_vis), t(top), K,
-                             t(swa), window, 1 / np.sqrt(512), out, abi.OUT_F32, lse, ws, ws.numel())
+                             t(swa), None, window, 1 / np.sqrt(512), out, abi.OUT_F32, lse, ws, ws.numel())
         torch.cuda.synchronize()
         st = abi.csa2_status_fetch(ws)
         assert st[0] == abi.ERR_DEVICE_BOUNDS and st[1] == 7 and st[2] == 2 and st[3] == 99
