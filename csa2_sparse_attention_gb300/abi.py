@@ -44,6 +44,8 @@ EXPORTS = {
     "csa2_index_reindex": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p, _p, _sz, _p]),
     "csa2_sparse_attn": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _p, _int, ctypes.c_float,
                                 _p, _int, _p, _p, _sz, _p]),
+    "csa2_index_reindex_noalloc": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p,
+                                          _p, _p]),
     "csa2_launch_count": (_i64, []),
     "csa2_kernel_name": (ctypes.c_char_p, [_int]),
     "csa2_timer_enable": (_int, [_int, _int]),
@@ -135,6 +137,17 @@ def csa2_index_reindex(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_
         _ptr(q_codes), _ptr(q_scales), _ptr(w), n_q, _ptr(k_codes), _ptr(k_scales), n_rows,
         _ptr(kv_start), _ptr(n_visible), max_visible, _ptr(pool), pool_blocks, topk, _ptr(out_topk),
         _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def csa2_index_reindex_noalloc(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible,
+                               max_visible, pool, pool_blocks, topk, out_topk, status, stream=None):
+    """csa2_index_reindex with the library's own fixed device scratch, for
+    callers that cannot allocate device memory; `status` is a device int32[4]
+    or None."""
+    return _check("csa2_index_reindex_noalloc", lib.csa2_index_reindex_noalloc(
+        _ptr(q_codes), _ptr(q_scales), _ptr(w), n_q, _ptr(k_codes), _ptr(k_scales), n_rows,
+        _ptr(kv_start), _ptr(n_visible), max_visible, _ptr(pool), pool_blocks, topk, _ptr(out_topk),
+        _ptr(status), _stream(stream)))
 
 
 def csa2_sparse_attn(q_bf16, n_q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa,

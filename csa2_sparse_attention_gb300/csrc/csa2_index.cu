@@ -804,3 +804,56 @@ extern "C" csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t*
     timer_end(K_SELECT_TOPK, s);
     return launch_status();
 }
+
+// ------------------------------------------------------------ no-allocation variant
+// csa2_index_reindex for callers that cannot allocate device memory (an
+// allocator-less runtime, a caller whose memory budget is fixed up front, or
+// code running where cudaMalloc is not allowed).  The per-position score
+// scratch lives in a fixed library-owned device array instead of a
+// caller-provided workspace.
+namespace csa2 {
+constexpr int64_t kNoallocScoreFloats = int64_t(512) * 1024;  // 2 MiB of fp32 scores
+static __device__ __align__(256) float g_noalloc_scores[kNoallocScoreFloats];
+static float* g_noalloc_ptr[64] = {};  // device address of g_noalloc_scores, per device
+}  // namespace csa2
+
+extern "C" csa2_status csa2_index_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales,
+                                                  const float* w, int64_t n_q, const uint8_t* k_codes,
+                                                  const uint8_t* k_scales, int64_t n_rows,
+                                                  const int64_t* kv_start, const int32_t* n_visible,
+                                                  int32_t max_visible, const int32_t* pool,
+                                                  int pool_blocks, int topk, int32_t* out_topk,
+                                                  int32_t* status, csa2_stream_t stream) {
+    csa2_status e = check_index_args(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start,
+                                     n_visible, max_visible, pool_blocks, topk);
+    if (e != CSA2_OK) return e;
+    if (!pool || !out_topk) return CSA2_ERR_INVALID_ARG;
+    if (status && (reinterpret_cast<uintptr_t>(status) & 3)) return CSA2_ERR_INVALID_ARG;
+    if (n_q * 8 * int64_t(pool_blocks) > kNoallocScoreFloats) return CSA2_ERR_UNSUPPORTED;
+    if (n_q == 0) return CSA2_OK;
+    if ((e = prepare_select_kernels()) != CSA2_OK) return e;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
+    if (g_noalloc_ptr[dev] == nullptr) {  // first call on this device: resolve the array's address
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scores) != cudaSuccess || p == nullptr) return CSA2_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    float* scores = g_noalloc_ptr[dev];
+    const int64_t stride = 8 * int64_t(pool_blocks);
+    Status* st = reinterpret_cast<Status*>(status);
+    cudaStream_t s = cudaStream_t(stream);
+    dim3 pgrid(unsigned(ceil_div(pool_blocks, kPoolBlocksPerCta)), unsigned(n_q));
+    timer_begin(K_POOL_SCORE, s);
+    pool_score_kernel<<<pgrid, kPoolWarps * 32, 0, s>>>(q_codes, q_scales, w, k_codes, k_scales, n_rows,
+                                                        kv_start, n_visible, max_visible, pool,
+                                                        pool_blocks, pool_blocks, scores, stride, st, true);
+    timer_end(K_POOL_SCORE, s);
+    const int cap_t = sel_cap(stride);
+    timer_begin(K_SELECT_TOPK, s);
+    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + pool_blocks) * 4, s>>>(
+        scores, stride, pool, pool_blocks, pool_blocks, kv_start, n_visible, max_visible, n_rows, topk,
+        out_topk, topk, cap_t);
+    timer_end(K_SELECT_TOPK, s);
+    return launch_status();
+}

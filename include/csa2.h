@@ -196,6 +196,34 @@ csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t* q_scales, 
                                int32_t* out_topk, void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /*
+ * csa2_index_reindex without a workspace, for callers that cannot allocate
+ * device memory: runtimes without a device allocator, callers whose memory
+ * is fixed before the model starts, or code running where cudaMalloc is not
+ * permitted.  The pages describe nothing like it; it exists only for such
+ * callers.  Arguments and results are those of csa2_index_reindex, except:
+ *   - the per-position scores go to one library-owned device array of 2 MiB
+ *     (held by every GPU that loads the library until the process exits):
+ *     n_q * 8 * pool_blocks must be at most 524,288, else the call returns
+ *     CSA2_ERR_UNSUPPORTED without launching (e.g. 32 queries at 2048 pool
+ *     blocks);
+ *   - status: a caller-owned device int32[4] that receives the first
+ *     device-detected problem (as the status word of a workspace), or NULL.
+ *     It is not cleared by the call.
+ * The first call on a device looks up the array's device address (one
+ * runtime query); make that first call before any stream capture.  Every
+ * call shares the array, whose contents are fully rewritten by each call;
+ * calls that overlap on the GPU (other streams, other threads) race on it.
+ * The call allocates nothing.
+ */
+csa2_status csa2_index_reindex_noalloc(const uint8_t* q_codes, const uint8_t* q_scales,
+                                       const float* w, int64_t n_q, const uint8_t* k_codes,
+                                       const uint8_t* k_scales, int64_t n_rows,
+                                       const int64_t* kv_start, const int32_t* n_visible,
+                                       int32_t max_visible, const int32_t* pool, int pool_blocks,
+                                       int topk, int32_t* out_topk, int32_t* status,
+                                       csa2_stream_t stream);
+
+/*
  * Sparse attention with one merged softmax ([T1] §二: 64 heads over a
  * 512-dim latent, every layer has its own Q and window KV; [T3] 第三刀: FP4
  * main KV dequantized before attention, window kept in FP8).  For query t,
