@@ -581,7 +581,10 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     const uint16_t* q = static_cast<const uint16_t*>(q_bf16);
     const uint16_t* sn = static_cast<const uint16_t*>(swa_new_bf16);
     const bool f32 = out_dtype == CSA2_OUT_F32;
-    const bool cluster = L.splits <= 8;  // portable cluster size: merge through shared memory
+    // merge through cluster shared memory only when every cluster of the
+    // launch can be resident at once (a cluster needs `splits` free SMs in
+    // one GPC); otherwise clusters run in waves and the workspace merge wins
+    const bool cluster = L.splits <= 8 && n_q * L.splits <= 64;
     const dim3 grid(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q));
     csa2_status e = CSA2_OK;
 #define CSA2_SPLIT(E_, C_)                                                                              \

@@ -333,6 +333,7 @@ struct SelShared {
     int hist[256];
     int wsum[3][kSelWarps];
     int misc[kSelWarps];
+    int bins[kSelWarps][32];
     uint32_t cand_key[kCandCap];
 };
 
@@ -462,24 +463,15 @@ __device__ void radix_threshold(const KeySrc& key, int n, int count, uint32_t& t
     take_eq = remaining;
 }
 
-// Block-wide sum over the 1024 threads; every thread gets the total.
-__device__ __forceinline__ int block_sum(int v, int* red) {
-    const int lane = lane_id(), warp = threadIdx.x >> 5;
-    v = __reduce_add_sync(0xffffffffu, v);
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    int t = __reduce_add_sync(0xffffffffu, lane < int(blockDim.x >> 5) ? red[lane] : 0);
-    __syncthreads();
-    return t;
-}
-
-// Threshold by binary search over the key range with the keys held in
-// registers (KPT per thread, n <= KPT * 1024): the largest T with
-// count(key >= T) >= count, then take_eq = count - count(key > T).
-// At most 32 steps of KPT compares and one block sum each.
+// Threshold by a 32-way search over the key range with the keys held in
+// registers (KPT per thread, n <= KPT * 1024).  Each round splits the live
+// range [lo, hi] into 32 buckets of 2^shift keys, counts the keys per bucket
+// (per-warp histograms), and keeps the bucket holding the count-th largest
+// key; `above` counts the keys beyond the live range.  At most 7 rounds of
+// two barriers end with lo == hi == T, take_eq = count - above.
 template <int KPT>
-__device__ void bsearch_threshold(const uint32_t* keys, int n, int count, uint32_t& thr, int& take_eq,
-                                  SelShared& sm) {
+__device__ void kary_threshold(const uint32_t* keys, int n, int count, uint32_t& thr, int& take_eq,
+                               SelShared& sm) {
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
     uint32_t k[KPT];
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -501,21 +493,50 @@ __device__ void bsearch_threshold(const uint32_t* keys, int n, int count, uint32
     __syncthreads();
     uint32_t lo = uint32_t(__reduce_min_sync(0xffffffffu, sm.wsum[0][lane])) ^ 0x80000000u;
     uint32_t hi = uint32_t(__reduce_max_sync(0xffffffffu, sm.wsum[1][lane])) ^ 0x80000000u;
+    int above = 0;
+    // per-warp 32-bin histograms: sm.bins[warp][bin]
+    for (int i = tid; i < kSelWarps * 32; i += blockDim.x) sm.bins[i >> 5][i & 31] = 0;
     __syncthreads();
     while (lo < hi) {
-        const uint32_t mid = lo + uint32_t((uint64_t(hi) - lo + 1) >> 1);
-        int c = 0;
+        const uint32_t width = hi - lo;
+        const int bits = 32 - __clz(width);           // width < 2^bits
+        const int shift = bits > 5 ? bits - 5 : 0;    // (width >> shift) < 32
 #pragma unroll
-        for (int j = 0; j < KPT; ++j) c += k[j] >= mid;
-        if (block_sum(c, sm.misc) >= count) lo = mid;
-        else hi = mid - 1;
+        for (int j = 0; j < KPT; ++j)
+            if (k[j] >= lo && k[j] <= hi) atomicAdd(&sm.bins[warp][(k[j] - lo) >> shift], 1);
+        __syncthreads();
+        if (warp == 0) {
+            int c = 0;
+            for (int w = 0; w < kSelWarps; ++w) {
+                c += sm.bins[w][lane];
+                sm.bins[w][lane] = 0;  // ready for the next round
+            }
+            // suffix sums from the top bucket down
+            int suf = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += y;
+            }
+            const unsigned ok = __ballot_sync(0xffffffffu, above + suf >= count);
+            const int bsel = 31 - __clz(ok);  // highest bucket still holding the threshold
+            const int suf_next = __shfl_sync(0xffffffffu, suf, (bsel + 1) & 31);
+            if (lane == 0) {
+                sm.misc[0] = bsel;
+                sm.misc[1] = above + (bsel < 31 ? suf_next : 0);
+            }
+        }
+        __syncthreads();
+        const uint32_t b = uint32_t(sm.misc[0]);
+        above = sm.misc[1];
+        const uint32_t nlo = lo + (b << shift);
+        const uint32_t nhi = nlo + ((1u << shift) - 1u);
+        lo = nlo;
+        hi = nhi < hi ? nhi : hi;
+        __syncthreads();
     }
-    int gt = 0;
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) gt += k[j] > lo;
-    gt = block_sum(gt, sm.misc);
     thr = lo;
-    take_eq = count - gt;
+    take_eq = count - above;
 }
 
 // Select `count` of n keys and write out[j] = map(i) for the selected i in
@@ -533,11 +554,11 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
     int take_eq = n;  // count == n: every key (all are >= 0) is taken
     if (count < n) {
         if (key.s && n <= 8 * kSelThreads)
-            bsearch_threshold<8>(key.s, n, count, thr, take_eq, sm);
+            kary_threshold<8>(key.s, n, count, thr, take_eq, sm);
         else if (key.s && n <= 16 * kSelThreads)
-            bsearch_threshold<16>(key.s, n, count, thr, take_eq, sm);
+            kary_threshold<16>(key.s, n, count, thr, take_eq, sm);
         else if (key.s && n <= 32 * kSelThreads)
-            bsearch_threshold<32>(key.s, n, count, thr, take_eq, sm);
+            kary_threshold<32>(key.s, n, count, thr, take_eq, sm);
         else
             radix_threshold(key, n, count, thr, take_eq, sm);
     }
@@ -545,12 +566,13 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
     const int seg = ((n + kSelWarps - 1) / kSelWarps + 31) & ~31;
     const int lo = min(n, warp * seg), hi = min(n, lo + seg);
     int gt = 0, eq = 0;
-    for (int b = lo; b < hi; b += 32) {
-        const int i = b + lane;
-        const uint32_t k = i < hi ? key(i) : 0u;
-        gt += __popc(__ballot_sync(0xffffffffu, i < hi && k > thr));
-        eq += __popc(__ballot_sync(0xffffffffu, i < hi && k == thr));
+    for (int i = lo + lane; i < hi; i += 32) {
+        const uint32_t k = key(i);
+        gt += k > thr;
+        eq += k == thr;
     }
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
     if (lane == 0) {
         sm.wsum[0][warp] = gt;
         sm.wsum[1][warp] = eq;
@@ -580,16 +602,35 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
     }
     __syncthreads();
     int eq_run = sm.wsum[1][warp], out_run = sm.wsum[2][warp];
-    for (int b = lo; b < hi; b += 32) {
-        const int i = b + lane;
-        const uint32_t k = i < hi ? key(i) : 0u;
-        const bool is_eq = i < hi && k == thr;
-        const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
-        const bool sel = (i < hi && k > thr) || (is_eq && eq_run + __popc(eqm & lanemask_lt()) < take_eq);
-        const unsigned sm_ = __ballot_sync(0xffffffffu, sel);
-        if (sel) out[out_run + __popc(sm_ & lanemask_lt())] = map(i);
-        eq_run += __popc(eqm);
-        out_run += __popc(sm_);
+    const unsigned lt = lanemask_lt();
+    constexpr int U = 4;  // chunks whose ballots are in flight together
+    for (int b = lo; b < hi; b += 32 * U) {
+        uint32_t kk[U];
+        bool in[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = b + 32 * u + lane;
+            in[u] = i < hi;
+            kk[u] = in[u] ? key(i) : 0u;
+        }
+        unsigned eqm[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) eqm[u] = __ballot_sync(0xffffffffu, in[u] && kk[u] == thr);
+        unsigned selm[U];
+        int er = eq_run;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool is_eq = (eqm[u] >> lane) & 1u;
+            const bool sel = (in[u] && kk[u] > thr) || (is_eq && er + __popc(eqm[u] & lt) < take_eq);
+            selm[u] = __ballot_sync(0xffffffffu, sel);
+            er += __popc(eqm[u]);
+        }
+        eq_run = er;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if ((selm[u] >> lane) & 1u) out[out_run + __popc(selm[u] & lt)] = map(b + 32 * u + lane);
+            out_run += __popc(selm[u]);
+        }
     }
     for (int i = count + tid; i < pad_to; i += blockDim.x) out[i] = -1;
 }
@@ -615,8 +656,16 @@ __global__ void __launch_bounds__(kSelThreads) select_blocks_kernel(
     const int nb = (n + 7) >> 3;
     const float* v = blockmax + q * nb_stride;
     KeySrc key{v, nullptr};
-    if (nb <= smem_keys_cap) {
-        for (int i = threadIdx.x; i < nb; i += blockDim.x) smem_keys[i] = float_key(v[i]);
+    if (nb <= smem_keys_cap) {  // rows start 16-byte aligned (nb_stride % 4 == 0)
+        const float4* v4 = reinterpret_cast<const float4*>(v);
+        for (int i = threadIdx.x; i < nb / 4; i += blockDim.x) {
+            const float4 x = v4[i];
+            smem_keys[4 * i] = float_key(x.x);
+            smem_keys[4 * i + 1] = float_key(x.y);
+            smem_keys[4 * i + 2] = float_key(x.z);
+            smem_keys[4 * i + 3] = float_key(x.w);
+        }
+        for (int i = (nb & ~3) + threadIdx.x; i < nb; i += blockDim.x) smem_keys[i] = float_key(v[i]);
         key.s = smem_keys;
         __syncthreads();
     }
@@ -653,8 +702,15 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     const int m = 8 * C;
     const float* v = scores + q * score_stride;
     KeySrc key{v, nullptr};
-    if (m <= smem_keys_cap) {
-        for (int i = threadIdx.x; i < m; i += blockDim.x) keys[i] = float_key(v[i]);
+    if (m <= smem_keys_cap) {  // m = 8C: whole float4s, 16-byte aligned rows
+        const float4* v4 = reinterpret_cast<const float4*>(v);
+        for (int i = threadIdx.x; i < m / 4; i += blockDim.x) {
+            const float4 x = v4[i];
+            keys[4 * i] = float_key(x.x);
+            keys[4 * i + 1] = float_key(x.y);
+            keys[4 * i + 2] = float_key(x.z);
+            keys[4 * i + 3] = float_key(x.w);
+        }
         key.s = keys;
     }
     __syncthreads();
