@@ -50,20 +50,8 @@ __host__ __device__ inline ReindexWs reindex_ws(int64_t n_q, int P) {
     return w;
 }
 
-// csa2_sparse_attn: entries per CTA (a multiple of 16, at most 80), chosen
-// so the split grid fills whole waves of one CTA per SM; cost model: waves x
-// (entries + 64 entry-equivalents of fixed per-CTA work).
-__host__ __device__ inline int attn_entries_per_cta(int64_t n_q, int total) {
-    int best = 80;
-    int64_t best_cost = -1;
-    for (int e = 80; e >= 16; e -= 16) {
-        if ((total + e - 1) / e > 128) break;  // the merge combines at most 128 splits
-        const int64_t ctas = n_q * ((total + e - 1) / e);
-        const int64_t cost = ((ctas + kSMs - 1) / kSMs) * (e + 64);
-        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = e; }
-    }
-    return best;
-}
+// csa2_sparse_attn: 128 entries per CTA (the M of the tensor-core tile).
+constexpr int kAttnEntries = 128;
 
 // split partials: O fp32 [64][512] and (m, l) per head per split
 struct AttnWs {
@@ -73,7 +61,7 @@ struct AttnWs {
 __host__ __device__ inline AttnWs attn_ws(int64_t n_q, int k, int window) {
     AttnWs w{};
     const int total = k + window;
-    w.entries = attn_entries_per_cta(n_q, total > 0 ? total : 1);
+    w.entries = kAttnEntries;
     w.splits = (total + w.entries - 1) / w.entries;
     if (w.splits < 1) w.splits = 1;
     w.part_o = CSA2_STATUS_BYTES;
