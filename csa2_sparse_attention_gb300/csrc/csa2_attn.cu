@@ -13,11 +13,15 @@
 // (M = 128 entries, N = 64 heads, K = 512, bf16, fp32 accumulate in TMEM),
 // stages S through shared memory for the split's softmax statistics (m, l),
 // and computes O^T = C^T P^T (M = 4 x 128 dims, N = 64 heads, K = 128
-// entries) with C converted in place to f16 (exact) and P split into f16
-// hi + lo parts, so the partial output carries ~2^-22 relative error.  One
-// shared-memory copy of C serves both products: K-major for the first,
-// MN-major for the second.  A merge kernel combines the splits with their
-// log-sum-exp weights and rounds once, to fp32 or bf16.
+// entries) with P split into bf16 hi + lo parts (the partial output carries
+// ~2^-17 relative error).  One shared-memory copy of C serves both products:
+// K-major for the first, MN-major for the second.  The splits of a query
+// form one thread-block cluster when all clusters of the launch can be
+// resident together: each CTA parks its fp32 partial in its own shared
+// memory and reduces one slice of the dims over its peers through
+// distributed shared memory.  Otherwise the partials go to the workspace and
+// a merge kernel combines them.  Either way the result is rounded once, to
+// fp32 or bf16.
 //
 // Optionally the kernel also appends the current token's window latent: the
 // bf16 row for position n-1 is rounded to E4M3 (as csa2_quantize_append FP8
@@ -28,6 +32,8 @@
 #include "csa2_tc.cuh"
 
 #include <cfloat>
+
+#include <cooperative_groups.h>
 
 namespace csa2 {
 
@@ -44,6 +50,8 @@ struct AttnTcSmem {
     uint32_t lut4[256];            // E2M1 pair -> bf16x2 (unscaled)
     uint16_t lut8[256];            // E4M3 byte -> bf16
     int ok[kTcE];                  // entry valid
+    float ml[kH][2];               // this split's (m, l) per head
+    float wts[kH][8];              // cluster merge weights a_s / L per head and split
     uint64_t bar;                  // MMA completion (phase 0: S, phase 1: O)
     uint32_t tmem;
 };
@@ -51,7 +59,7 @@ struct AttnTcSmem {
 // canonical no-swizzle K-major offsets: rows of 512 16-bit elements, 16-byte
 // chunk c of row r -> (r/8)*8192 + c*128 + (r%8)*16
 __device__ __forceinline__ uint32_t row512(int r, int c) { return uint32_t((r >> 3) * 8192 + c * 128 + (r & 7) * 16); }
-// P [64 heads][128 entries] f16, K-major
+// P [64 heads][128 entries] bf16, K-major
 __device__ __forceinline__ uint32_t poff(int h, int e) {
     return uint32_t((h >> 3) * 2048 + (e >> 3) * 128 + (h & 7) * 16 + (e & 7) * 2);
 }
@@ -76,21 +84,28 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// grid (splits, n_q), 256 threads, one CTA per SM.  Writes the split's
-// unnormalized partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [64][512]) and
-// (m_s, l_s) per head to the workspace.
+// grid (splits, n_q), 256 threads, one CTA per SM.  The split's unnormalized
+// partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [64][512]) and (m_s, l_s) per
+// head go to the workspace, or (CLUSTER) are merged across the cluster.
+template <bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const uint16_t* __restrict__ qg, const uint8_t* __restrict__ kv_codes,
     const uint8_t* __restrict__ kv_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, const int32_t* __restrict__ topk, int k,
     uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, float sm_scale,
-    float* __restrict__ part_o, float* __restrict__ part_ml, int splits, Status* st) {
+    float* __restrict__ part_o, float* __restrict__ part_ml, int splits, void* __restrict__ out,
+    bool out_f32, float* __restrict__ out_lse, Status* st) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     AttnTcSmem& S = *reinterpret_cast<AttnTcSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
     const int split = blockIdx.x;
     const int64_t q = blockIdx.y;
 
+    // the query's row range and this thread's two top-k entries, first
+    const int64_t ks = kv_start[q];
+    const int32_t nv = n_visible[q];
+    const int pre_ge = split * kTcE + (tid & (kTcE - 1));  // this thread's entry (both items)
+    const int32_t pre = pre_ge < k ? topk[q * k + pre_ge] : -1;
     if (tid == 0) {
         mbar_init(&S.bar, 1);
         mbar_init_fence();
@@ -111,9 +126,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         S.lut8[b] = bf16_bits(e4m3_value(uint32_t(b)));
     }
     int32_t n = 0;  // per-query validity, reported once per query
-    const int64_t ks = kv_start[q];
     {
-        const int32_t nv = n_visible[q];
         const bool report = split == 0 && tid == 0;
         if (ks < 0) {
             if (report) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_KV_START, int32_t(q), int32_t(ks));
@@ -126,13 +139,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const int nw = n < window ? n : window;
     __syncthreads();  // tables ready
 
-    // gather + dequantize: item -> (entry e = item/4, quarter qq = item%4)
+    // gather + dequantize: item -> (entry e = item % 128, quarter qq = item / 128);
+    // consecutive lanes take consecutive entries, so each 16-byte store of a
+    // warp phase lands on distinct banks
     for (int item = tid; item < kTcE * 4; item += kAttnThreads) {
-        const int e = item >> 2, qq = item & 3;
+        const int e = item & (kTcE - 1), qq = item >> 7;
         const int ge = split * kTcE + e;
         bool ok = false;
         if (ge < k) {
-            const int32_t p = topk[q * k + ge];
+            const int32_t p = pre;
             if (p >= 0 && p < n) {
                 ok = true;
                 const int64_t row = ks + p;
@@ -243,8 +258,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     __syncthreads();
 
     // softmax statistics: thread -> (head tid/4, entries c0, c0+4, ...)
-    __half* p_hi = reinterpret_cast<__half*>(S.r0 + 32 * 1024);
-    __half* p_lo = reinterpret_cast<__half*>(S.r0 + 48 * 1024);
+    uint8_t* p_hi = S.r0 + 32 * 1024;
+    uint8_t* p_lo = S.r0 + 48 * 1024;
     {
         constexpr int PER = kTcE / 4;
         const int h = tid >> 2, c0 = tid & 3;
@@ -261,27 +276,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int e = c0 + 4 * j;
-            const float p = x[j] == -INFINITY ? 0.f : expf(x[j] - m);
+            const float p = x[j] == -INFINITY ? 0.f : __expf(x[j] - m);
             l += p;
-            const __half hi = __float2half_rn(p);
-            *reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(p_hi) + poff(h, e)) = hi;
-            *reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(p_lo) + poff(h, e)) =
-                __float2half_rn(p - __half2float(hi));
+            const uint16_t hi = bf16_bits(p);
+            *reinterpret_cast<uint16_t*>(p_hi + poff(h, e)) = hi;
+            *reinterpret_cast<uint16_t*>(p_lo + poff(h, e)) = bf16_bits(p - __uint_as_float(uint32_t(hi) << 16));
         }
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
         if (c0 == 0) {
-            float* ml = part_ml + ((q * splits + split) * kH + h) * 2;
-            ml[0] = m;
-            ml[1] = l;
-        }
-    }
-    {  // C from bf16 to f16 in place (exact for FP4 and E4M3 values)
-        uint32_t* cw = reinterpret_cast<uint32_t*>(S.c);
-        for (int i = tid; i < kTcE * kD / 2; i += kAttnThreads) {
-            const uint32_t v = cw[i];
-            const __half2 h = __floats2half2_rn(bf16_lo(v), bf16_hi(v));
-            cw[i] = *reinterpret_cast<const uint32_t*>(&h);
+            if (CLUSTER) {
+                S.ml[h][0] = m;
+                S.ml[h][1] = l;
+            } else {
+                float* ml = part_ml + ((q * splits + split) * kH + h) * 2;
+                ml[0] = m;
+                ml[1] = l;
+            }
         }
     }
     fence_async_smem();
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 
     // O^T = C^T P^T: 4 blocks of 128 dims; C is the MN-major A operand
     if (tid == 0 && ok_mma) {
-        constexpr uint32_t id = idesc_f16(128, 64, 0, true, false);
+        constexpr uint32_t id = idesc_f16(128, 64, 1, true, false);
         const uint32_t ph = smem_addr(p_hi), pl = smem_addr(p_lo);
         for (int mb = 0; mb < 4; ++mb) {
             const uint32_t d = tmem + 64 + 64 * mb;
@@ -306,8 +317,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     }
     if (ok_mma) ok_mma = mbar_wait(&S.bar, 1);
     tc_fence_after();
-    if (ok_mma) {  // warp -> dims 32*(warp%4) + lane of blocks 2*(warp/4), +1
-        float* out = part_o + (q * splits + split) * int64_t(kH * kD);
+    // warp -> dims 32*(warp%4) + lane of blocks 2*(warp/4), +1: to the
+    // workspace, or (CLUSTER) to this CTA's shared memory (C is consumed)
+    float* X = CLUSTER ? reinterpret_cast<float*>(S.c) : part_o + (q * splits + split) * int64_t(kH * kD);
+    if (ok_mma) {
         for (int b2 = 0; b2 < 2; ++b2) {
             const int mb = 2 * (warp >> 2) + b2;
             const int dim = mb * 128 + 32 * (warp & 3) + lane;
@@ -317,11 +330,75 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
                 tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + 64 + 64 * mb + 32 * half, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) out[(32 * half + j) * kD + dim] = __uint_as_float(r[j]);
+                for (int j = 0; j < 32; ++j) X[(32 * half + j) * kD + dim] = __uint_as_float(r[j]);
             }
         }
     } else if (tid == 0) {
         record(st, CSA2_ERR_TIMEOUT, 2, int32_t(q), split);
+    }
+    if (CLUSTER) {
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every partial and (m, l) of the query is visible
+        const int rank = int(cluster.block_rank());
+        if (tid < kH) {  // merge weights of head tid
+            float mp[8], lp[8], M = -INFINITY;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                mp[p] = -INFINITY;
+                lp[p] = 0.f;
+                if (p < splits) {
+                    const float2 v = *reinterpret_cast<const float2*>(cluster.map_shared_rank(&S.ml[tid][0], p));
+                    mp[p] = v.x;
+                    lp[p] = v.y;
+                }
+                M = fmaxf(M, mp[p]);
+            }
+            float L = 0.f, a[8];
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                a[p] = (M == -INFINITY || mp[p] == -INFINITY) ? 0.f : __expf(mp[p] - M);
+                L = fmaf(a[p], lp[p], L);
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) S.wts[tid][p] = a[p] * inv;
+            if (rank == 0 && out_lse) out_lse[q * kH + tid] = L > 0.f ? M + logf(L) : -INFINITY;
+        }
+        __syncthreads();
+        // this CTA reduces dims [lo, hi) (whole float4s) over all peers
+        const int per = ((kD / 4 + splits - 1) / splits) * 4;
+        const int lo = rank * per, hi = min(kD, lo + per);
+        const int w4 = (hi - lo) / 4;
+        const float4* px[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+            px[p] = reinterpret_cast<const float4*>(cluster.map_shared_rank(X, p < splits ? p : 0));
+        for (int idx = tid; idx < kH * w4; idx += kAttnThreads) {
+            const int h = idx / w4, d4 = lo / 4 + idx % w4;
+            float4 v[8];
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+                v[p] = p < splits ? px[p][h * (kD / 4) + d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const float wgt = p < splits ? S.wts[h][p] : 0.f;
+                o.x = fmaf(wgt, v[p].x, o.x);
+                o.y = fmaf(wgt, v[p].y, o.y);
+                o.z = fmaf(wgt, v[p].z, o.z);
+                o.w = fmaf(wgt, v[p].w, o.w);
+            }
+            const int64_t oi = (q * kH + h) * int64_t(kD) + 4 * d4;
+            if (out_f32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(out) + oi) = o;
+            } else {
+                const uint32_t a0 = uint32_t(bf16_bits(o.x)) | (uint32_t(bf16_bits(o.y)) << 16);
+                const uint32_t a1 = uint32_t(bf16_bits(o.z)) | (uint32_t(bf16_bits(o.w)) << 16);
+                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + oi) = make_uint2(a0, a1);
+            }
+        }
+        cluster.sync();  // peers are done reading this CTA's shared memory
     }
     tc_fence_before();
     __syncthreads();
@@ -413,16 +490,41 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     if (lse && lane == 0) lse[q * kH + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
-static csa2_status prepare_attn_tc() {
+// Opt both variants into their shared memory and note how many clusters of
+// `splits` CTAs can be resident at once (0 when clusters are unavailable).
+static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
     static bool done[64] = {};
+    static int cached[64][9] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
     if (!done[dev]) {
-        if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(AttnTcSmem))) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnTcSmem))) != cudaSuccess)
             return CSA2_ERR_CUDA;
+        for (int c = 1; c <= 8; ++c) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(unsigned(c), 1, 1);
+            cfg.blockDim = dim3(kAttnThreads, 1, 1);
+            cfg.dynamicSmemBytes = sizeof(AttnTcSmem);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = unsigned(c);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<true>, &cfg) != cudaSuccess) {
+                n = 0;
+                cudaGetLastError();
+            }
+            cached[dev][c] = n;
+        }
         done[dev] = true;
     }
+    *max_clusters = (splits >= 1 && splits <= 8) ? cached[dev][splits] : 0;
     return CSA2_OK;
 }
 
@@ -460,14 +562,35 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     const uint16_t* q = static_cast<const uint16_t*>(q_bf16);
     const uint16_t* sn = static_cast<const uint16_t*>(swa_new_bf16);
     const bool f32 = out_dtype == CSA2_OUT_F32;
-    csa2_status e = prepare_attn_tc();
+    int max_clusters = 0;
+    csa2_status e = prepare_attn_tc(L.splits, &max_clusters);
     if (e != CSA2_OK) return e;
-    const dim3 grid(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q));
+    // one cluster per query when every cluster of the launch is resident at once
+    const bool cluster = L.splits <= 8 && n_q <= max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q), 1);
+    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(AttnTcSmem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (cluster) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(L.splits);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     timer_begin(K_ATTN_SPLIT, s);
-    attn_tc_kernel<<<grid, kAttnThreads, sizeof(AttnTcSmem), s>>>(q, kv_codes, kv_scales, n_rows, kv_start,
-                                                                   n_visible, topk, k, swa, sn, window, sm_scale,
-                                                                   part_o, part_ml, L.splits, st);
+    const cudaError_t le =
+        cluster ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, q, kv_codes, kv_scales, n_rows, kv_start, n_visible,
+                                     topk, k, swa, sn, window, sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st)
+                : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, q, kv_codes, kv_scales, n_rows, kv_start,
+                                     n_visible, topk, k, swa, sn, window, sm_scale, part_o, part_ml, L.splits, out,
+                                     f32, out_lse, st);
     timer_end(K_ATTN_SPLIT, s);
+    if (le != cudaSuccess) return CSA2_ERR_CUDA;
+    if (cluster) return launch_status();
     timer_begin(K_ATTN_MERGE, s);
     if (f32)
         attn_merge_kernel<true><<<dim3(unsigned(n_q), kH / 8), 256, 0, s>>>(part_o, part_ml, L.splits, out, out_lse);

@@ -10,128 +10,17 @@
 // Score (the pages give none; this library's definition):
 //   I(t,s) = sum_h w[t][h] * max(0, q~[t][h] . k~[s]),  32 heads x 128 dims.
 //
-// Scoring core (scan and pool): a warp scores 16 positions against all 32
-// heads with 32 m16n8k16 f16 MMAs.  Operands are FP4 dequantized in
-// registers: an E2M1 pair converts to f16x2 and is multiplied by its group's
-// E4M3 scale, both exact in f16 (at most 6 significant bits, magnitudes in
-// [2^-10, 2688]); products are exact and accumulate in fp32.  The reduction
-// index of each MMA is a permutation of channels shared by both operands, so
-// each thread reads one contiguous 16-byte chunk (32 channels) per row.
+// Scoring (scan and pool) runs on the 5th-generation tensor cores as block-
+// scaled FP4 MMAs (E2M1 operands, one E4M3 scale per 16 channels, fp32
+// accumulate in TMEM); the ReLU, head weights, head sum and block maximum
+// are applied to the accumulator in registers.
 #include "csa2_common.cuh"
 #include "csa2_timer.cuh"
 #include "csa2_layout.cuh"
 #include "csa2_pipe.cuh"
+#include "csa2_tc.cuh"
 
 namespace csa2 {
-
-// ------------------------------------------------------------ scoring core
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t byte_of(const uint4& v, int b) {
-    const uint32_t w = b < 4 ? v.x : b < 8 ? v.y : b < 12 ? v.z : v.w;
-    return (w >> (8 * (b & 3))) & 0xFF;
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t s) {
-    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&s));
-    return *reinterpret_cast<uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t scale_h2(uint32_t sbyte) {
-    __half2 h = __float2half2_rn(e4m3_value(sbyte));
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Byte offset of the 16-byte chunk c (channels 32c..32c+31) of row r in the
-// BLOCK8 layout.
-__device__ __forceinline__ int64_t block8_chunk(int64_t r, int c) {
-    return (r >> 3) * 512 + c * 128 + (r & 7) * 16;
-}
-
-// Indexer query of one query as MMA B fragments: [n-tile j][k-step kk][2].
-struct QFrag {
-    uint32_t b[4][8][2];
-    float w[4][2];
-};
-
-__device__ __forceinline__ void load_qfrag(QFrag& f, const uint8_t* __restrict__ q_codes,
-                                           const uint8_t* __restrict__ q_scales,
-                                           const float* __restrict__ w, int64_t q) {
-    const int lane = lane_id(), t = lane & 3, hn = lane >> 2;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t r = q * 32 + 8 * j + hn;
-        const uint4 c = __ldg(reinterpret_cast<const uint4*>(q_codes + block8_chunk(r, t)));
-        const uint32_t s0 = scale_h2(__ldg(q_scales + r * 8 + 2 * t));
-        const uint32_t s1 = scale_h2(__ldg(q_scales + r * 8 + 2 * t + 1));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t s = kk < 4 ? s0 : s1;
-            f.b[j][kk][0] = hmul2_u32(e2m1x2_to_f16x2(byte_of(c, 2 * kk)), s);
-            f.b[j][kk][1] = hmul2_u32(e2m1x2_to_f16x2(byte_of(c, 2 * kk + 1)), s);
-        }
-        f.w[j][0] = __ldg(w + q * 32 + 8 * j + 2 * t);
-        f.w[j][1] = __ldg(w + q * 32 + 8 * j + 2 * t + 1);
-    }
-}
-
-// Raw FP4 data of the two rows a thread feeds into one 16-position tile.
-struct KRaw {
-    uint4 c0, c1;
-    uint32_t s0, s1;  // two scale bytes (groups 2t, 2t+1) of each row
-};
-
-__device__ __forceinline__ void load_kraw(KRaw& k, const uint8_t* __restrict__ k_codes,
-                                          const uint8_t* __restrict__ k_scales, int64_t r0,
-                                          bool v0, int64_t r1, bool v1) {
-    const int t = lane_id() & 3;
-    k.c0 = v0 ? __ldg(reinterpret_cast<const uint4*>(k_codes + block8_chunk(r0, t))) : make_uint4(0, 0, 0, 0);
-    k.c1 = v1 ? __ldg(reinterpret_cast<const uint4*>(k_codes + block8_chunk(r1, t))) : make_uint4(0, 0, 0, 0);
-    k.s0 = v0 ? __ldg(reinterpret_cast<const uint16_t*>(k_scales + r0 * 8 + 2 * t)) : 0u;
-    k.s1 = v1 ? __ldg(reinterpret_cast<const uint16_t*>(k_scales + r1 * 8 + 2 * t)) : 0u;
-}
-
-// Scores of the tile's rows lane/4 (out0) and lane/4 + 8 (out1), full sums
-// over the 32 heads in every lane of the quad.
-__device__ __forceinline__ void score_tile(const QFrag& f, const KRaw& k, float& out0, float& out1) {
-    float acc[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    const uint32_t sa0 = scale_h2(k.s0 & 0xFF), sa1 = scale_h2((k.s0 >> 8) & 0xFF);
-    const uint32_t sb0 = scale_h2(k.s1 & 0xFF), sb1 = scale_h2((k.s1 >> 8) & 0xFF);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t s0 = kk < 4 ? sa0 : sa1, s1 = kk < 4 ? sb0 : sb1;
-        uint32_t a[4];
-        a[0] = hmul2_u32(e2m1x2_to_f16x2(byte_of(k.c0, 2 * kk)), s0);
-        a[1] = hmul2_u32(e2m1x2_to_f16x2(byte_of(k.c1, 2 * kk)), s1);
-        a[2] = hmul2_u32(e2m1x2_to_f16x2(byte_of(k.c0, 2 * kk + 1)), s0);
-        a[3] = hmul2_u32(e2m1x2_to_f16x2(byte_of(k.c1, 2 * kk + 1)), s1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mma16816(acc[j], a, f.b[j][kk][0], f.b[j][kk][1]);
-    }
-    float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        x0 = fmaf(f.w[j][0], fmaxf(acc[j][0], 0.f), x0);
-        x0 = fmaf(f.w[j][1], fmaxf(acc[j][1], 0.f), x0);
-        x1 = fmaf(f.w[j][0], fmaxf(acc[j][2], 0.f), x1);
-        x1 = fmaf(f.w[j][1], fmaxf(acc[j][3], 0.f), x1);
-    }
-    x0 += __shfl_xor_sync(0xffffffffu, x0, 1);
-    x1 += __shfl_xor_sync(0xffffffffu, x1, 1);
-    x0 += __shfl_xor_sync(0xffffffffu, x0, 2);
-    x1 += __shfl_xor_sync(0xffffffffu, x1, 2);
-    out0 = x0;
-    out1 = x1;
-}
 
 // Per-query validity shared by every index/attention kernel.
 __device__ __forceinline__ int32_t checked_visible(const int64_t* kv_start, const int32_t* n_visible,
@@ -154,165 +43,218 @@ __device__ __forceinline__ int32_t checked_visible(const int64_t* kv_start, cons
     return n;
 }
 
-// ------------------------------------------------------------ full scan
-// Producer/consumer pipeline.  One producer lane streams tiles of 128
-// positions (16 BLOCK8 blocks: 8 KB of codes, 1 KB of scales, each one
-// contiguous bulk copy) into a ring of kScanStages shared-memory stages;
-// eight consumer warps score 16 positions each per tile with the register
-// dequant + mma.sync core and write the block maxima.  CTA (x, q) scans a
-// contiguous range of query q's tiles.
-constexpr int kScanCW = 8;                       // consumer warps
-constexpr int kScanThreads = (kScanCW + 1) * 32;
-constexpr int kTile = 128;                       // positions per tile
-constexpr int kScanStages = 8;
+constexpr int kTile = 128;  // positions per tensor-core tile (16 blocks of 8)
 
-struct ScanSmem {
-    uint8_t codes[kScanStages][kTile * 64];
-    uint8_t scales[kScanStages][kTile * 8];
-    uint64_t full[kScanStages];
-    uint64_t empty[kScanStages];
+// ------------------------------------------------------------ tensor-core scorer
+// Block-scaled FP4 tcgen05 scorer shared by the full scan and the in-pool
+// scoring.  A tile is 16 blocks = 128 positions (M); N = 32 index heads;
+// K = 128 channels as two kind::mxf4nvf4 MMAs of 64 with one E4M3 scale per
+// 16 channels, so the FP4 codes go from shared memory to the tensor core
+// without dequantization.  Warp 0 streams tiles (contiguous blocks for the
+// scan, the candidate blocks for the pool) into a ring of shared-memory
+// stages with bulk copies; warp 1 issues the MMAs; warps 2..5 copy each
+// tile's scales into TMEM and reduce the 32 head scores of every position:
+// the block maxima (scan) or per-position scores (pool).
+constexpr int kTcThreads = 192;
+constexpr int kTcStages = 8;
+constexpr int kTcAcc = 4;            // accumulator stages (32 TMEM columns each)
+constexpr int kTcSf = 4;             // scale-factor slots (8 columns each)
+constexpr uint32_t kTcCols = 256;
+constexpr uint32_t kColAcc = 0, kColSfa = 128, kColSfb = 160;
+
+struct TcScanSmem {
+    uint8_t codes[kTcStages][kTile * 64];
+    uint8_t scales[kTcStages][kTile * 8];
+    uint8_t qcodes[32 * 64];          // the query's 32 heads, BLOCK8 = canonical K-major
+    uint64_t full[kTcStages], empty[kTcStages];
+    uint64_t sfa_ready[kTcSf];
+    uint64_t acc_full[kTcAcc], acc_empty[kTcAcc];
+    uint64_t qbar;
+    uint32_t tmem;
+    int abort_flag;
 };
 
-__global__ void __launch_bounds__(kScanThreads, 1) scan_blockmax_kernel(
-    const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales,
-    const float* __restrict__ w, const uint8_t* __restrict__ k_codes,
-    const uint8_t* __restrict__ k_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
-    const int32_t* __restrict__ n_visible, int32_t max_visible, float* __restrict__ blockmax,
-    int64_t nb_stride, int ctas_per_query, Status* st) {
-    extern __shared__ __align__(128) uint8_t scan_smem_raw[];
-    ScanSmem& S = *reinterpret_cast<ScanSmem*>(scan_smem_raw);
-    const int64_t q = blockIdx.y;
-    const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, st,
-                                      blockIdx.x == 0 && threadIdx.x == 0);
-    const int64_t tiles_q = (int64_t(n) + kTile - 1) / kTile;
-    const int64_t per = (tiles_q + ctas_per_query - 1) / ctas_per_query;
-    const int64_t t0 = int64_t(blockIdx.x) * per;
-    const int64_t t1 = t0 + per < tiles_q ? t0 + per : tiles_q;
-    if (t0 >= t1) return;  // uniform over the CTA
-    const int64_t ks = kv_start[q];
-    const int64_t nblk_vis = (int64_t(n) + 7) >> 3;
-    const int lane = lane_id(), warp = threadIdx.x >> 5;
-    const int ntiles = int(t1 - t0);
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kScanStages; ++s) {
-            mbar_init(&S.full[s], 1);
-            mbar_init(&S.empty[s], kScanCW);
-        }
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    if (warp == kScanCW) {  // producer
-        if (lane == 0) {
-            for (int i = 0; i < ntiles; ++i) {
-                const int s = i % kScanStages, r = i / kScanStages;
-                if (r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
-                    record(st, CSA2_ERR_TIMEOUT, 0, int32_t(q), i);
-                    break;
-                }
-                const int64_t t = t0 + i;
-                const int64_t nvb64 = nblk_vis - t * 16;
-                const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
-                mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
-                bulk_g2s(S.codes[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
-                bulk_g2s(S.scales[s], k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
-            }
-        }
-        return;
-    }
-
-    // consumers
-    QFrag f;
-    load_qfrag(f, q_codes, q_scales, w, q);
-    float* out = blockmax + q * nb_stride;
-    const int tq = lane & 3, rr = lane >> 2;
-    for (int i = 0; i < ntiles; ++i) {
-        const int s = i % kScanStages, r = i / kScanStages;
-        if (!mbar_wait(&S.full[s], r & 1)) {
-            if (lane == 0) record(st, CSA2_ERR_TIMEOUT, 1, int32_t(q), i);
-            break;
-        }
-        const int64_t t = t0 + i;
-        const int64_t b0 = t * 16 + 2 * warp;  // first of this warp's two blocks
-        const bool v0 = b0 < nblk_vis, v1 = b0 + 1 < nblk_vis;
-        if (v0) {
-            KRaw k;
-            const uint8_t* cb = S.codes[s] + (2 * warp) * 512 + tq * 128 + rr * 16;
-            const uint8_t* sb = S.scales[s] + ((2 * warp) * 8 + rr) * 8 + 2 * tq;
-            k.c0 = *reinterpret_cast<const uint4*>(cb);
-            k.s0 = *reinterpret_cast<const uint16_t*>(sb);
-            k.c1 = v1 ? *reinterpret_cast<const uint4*>(cb + 512) : make_uint4(0, 0, 0, 0);
-            k.s1 = v1 ? *reinterpret_cast<const uint16_t*>(sb + 64) : 0u;
-            float s0, s1;
-            score_tile(f, k, s0, s1);
-            const int64_t pos0 = b0 * 8 + rr, pos1 = pos0 + 8;
-            float m0 = pos0 < n ? s0 : -INFINITY;
-            float m1 = pos1 < n ? s1 : -INFINITY;
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-            }
-            if (lane == 0) {
-                out[b0] = m0;
-                if (v1) out[b0 + 1] = m1;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[s]);
-    }
-}
-
-// ------------------------------------------------------------ pool scoring
-constexpr int kPoolWarps = 8;
-constexpr int kPoolBlocksPerCta = 128;
-
-// grid (ceil(C / 128), n_q).  scores[q][8*i + r] = I(t, 8*cand[q][i] + r), or
-// -inf for a pad, an out-of-range block or a position >= n.
-__global__ void __launch_bounds__(kPoolWarps * 32) pool_score_kernel(
+template <bool GATHER>
+__global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales,
     const float* __restrict__ w, const uint8_t* __restrict__ k_codes,
     const uint8_t* __restrict__ k_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, const int32_t* __restrict__ cand,
-    int64_t cand_stride, int C, float* __restrict__ scores, int64_t score_stride, Status* st,
-    bool check_cand) {
+    int64_t cand_stride, int C, float* __restrict__ out, int64_t out_stride, int ctas_per_query,
+    bool check_cand, Status* st) {
+    extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
+    TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
     const int64_t q = blockIdx.y;
-    const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, st, false);
+    const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, GATHER ? nullptr : st,
+                                      !GATHER && blockIdx.x == 0 && threadIdx.x == 0);
+    const int64_t nblk_vis = (int64_t(n) + 7) >> 3;
+    const int64_t tiles_q = GATHER ? (C + 15) / 16 : (nblk_vis + 15) / 16;
+    const int64_t per = (tiles_q + ctas_per_query - 1) / ctas_per_query;
+    const int64_t t0 = int64_t(blockIdx.x) * per;
+    const int64_t t1 = t0 + per < tiles_q ? t0 + per : tiles_q;
+    if (n <= 0 || t0 >= t1) {
+        if (GATHER) {  // nothing visible: every score of this range is -inf
+            const int64_t end = t1 * 128 < 8 * int64_t(C) ? t1 * 128 : 8 * int64_t(C);
+            for (int64_t i = t0 * 128 + threadIdx.x; i < end; i += blockDim.x) out[q * out_stride + i] = -INFINITY;
+        }
+        return;
+    }
     const int64_t ks = kv_start[q];
-    const int64_t nb = (int64_t(n) + 7) >> 3;
+    const int32_t* cq = GATHER ? cand + q * cand_stride : nullptr;
     const int lane = lane_id(), warp = threadIdx.x >> 5;
-    const int i_begin = blockIdx.x * kPoolBlocksPerCta;
-    const int i_end = min(C, i_begin + kPoolBlocksPerCta);
-    float* out = scores + q * score_stride;
-    const int32_t* cq = cand + q * cand_stride;
-    QFrag f;
-    bool have_q = false;
-    for (int i = i_begin + 2 * warp; i < i_end; i += 2 * kPoolWarps) {
-        int64_t b0 = cq[i];
-        int64_t b1 = i + 1 < i_end ? cq[i + 1] : -1;
-        if (check_cand && lane == 0) {
-            if (b0 < -1 || b0 >= nb)
-                record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), int32_t(b0));
-            if (i + 1 < i_end && (b1 < -1 || b1 >= nb))
-                record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), int32_t(b1));
+    const int ntiles = int(t1 - t0);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], 1);
         }
-        const bool v0 = b0 >= 0 && b0 < nb, v1 = b1 >= 0 && b1 < nb;
-        float s0 = -INFINITY, s1 = -INFINITY;
-        if (v0 || v1) {
-            if (!have_q) {
-                load_qfrag(f, q_codes, q_scales, w, q);
-                have_q = true;
+        for (int f = 0; f < kTcSf; ++f) mbar_init(&S.sfa_ready[f], 128);
+        for (int a = 0; a < kTcAcc; ++a) {
+            mbar_init(&S.acc_full[a], 1);
+            mbar_init(&S.acc_empty[a], 128);
+        }
+        mbar_init(&S.qbar, 1);
+        S.abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) tmem_alloc(&S.tmem, kTcCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem;
+
+    if (warp == 0) {  // ------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&S.qbar, 32 * 64);
+            bulk_g2s(S.qcodes, q_codes + (q * 32 / 8) * 512, 32 * 64, &S.qbar);
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % kTcStages, r = i / kTcStages;
+                if (r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
+                    record(st, CSA2_ERR_TIMEOUT, 10, int32_t(q), i);
+                    S.abort_flag = 1;
+                    break;
+                }
+                const int64_t t = t0 + i;
+                if (!GATHER) {
+                    const int64_t nvb64 = nblk_vis - t * 16;
+                    const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
+                    mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
+                    bulk_g2s(S.codes[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
+                    bulk_g2s(S.scales[s], k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
+                } else {
+                    uint32_t bytes = 0;
+                    int32_t bl[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int64_t ci = t * 16 + j;
+                        bl[j] = ci < C ? cq[ci] : -1;
+                        if (bl[j] >= 0 && bl[j] < nblk_vis) bytes += 512 + 64;
+                        else if (check_cand && (bl[j] < -1 || bl[j] >= nblk_vis))
+                            record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), bl[j]);
+                    }
+                    mbar_arrive_expect_tx(&S.full[s], bytes);  // 0 bytes: the phase completes at once
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (bl[j] >= 0 && bl[j] < nblk_vis) {
+                            bulk_g2s(S.codes[s] + j * 512, k_codes + ((ks >> 3) + bl[j]) * 512, 512, &S.full[s]);
+                            bulk_g2s(S.scales[s] + j * 64, k_scales + (ks + 8 * int64_t(bl[j])) * 8, 64, &S.full[s]);
+                        }
+                    }
+                }
             }
-            KRaw k;
-            load_kraw(k, k_codes, k_scales, ks + 8 * b0 + (lane >> 2), v0, ks + 8 * b1 + (lane >> 2), v1);
-            score_tile(f, k, s0, s1);
         }
-        const int r = lane >> 2;
-        if ((lane & 3) == 0) {
-            out[8 * int64_t(i) + r] = (v0 && 8 * b0 + r < n) ? s0 : -INFINITY;
-            if (i + 1 < i_end) out[8 * int64_t(i + 1) + r] = (v1 && 8 * b1 + r < n) ? s1 : -INFINITY;
+    } else if (warp == 1) {  // ----------------------------------- MMA issue
+        if (lane == 0) {
+            bool ok = mbar_wait(&S.qbar, 0);
+            constexpr uint32_t id = idesc_mxf4nvf4(128, 32);
+            const uint32_t qa = smem_u32(S.qcodes);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int s = i % kTcStages, f = i % kTcSf, a = i % kTcAcc;
+                ok = mbar_wait(&S.full[s], (i / kTcStages) & 1) && mbar_wait(&S.sfa_ready[f], (i / kTcSf) & 1) &&
+                     (i < kTcAcc || mbar_wait(&S.acc_empty[a], ((i / kTcAcc) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(S.codes[s]);
+                const uint32_t d = tmem + kColAcc + 32 * a;
+                const uint32_t sfa = tmem + kColSfa + 8 * f, sfb = tmem + kColSfb;
+                mma_mxf4_ss(d, umma_desc(ka, 128, 512), umma_desc(qa, 128, 512), id, sfa, sfb, false);
+                mma_mxf4_ss(d, umma_desc(ka + 256, 128, 512), umma_desc(qa + 256, 128, 512), id, sfa + 4, sfb + 4, true);
+                tc_commit(&S.acc_full[a]);
+                tc_commit(&S.empty[s]);
+            }
+            if (!ok) {
+                record(st, CSA2_ERR_TIMEOUT, 11, int32_t(q), 0);
+                S.abort_flag = 1;
+            }
+        }
+    } else {  // --------------------------------------------------- epilogue
+        const int quad = warp & 3;              // TMEM lane quadrant of this warp
+        const int row = 32 * quad + lane;       // position within a tile
+        const uint32_t lane_base = tmem + (uint32_t(32 * quad) << 16);
+        float wv[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) wv[h] = __ldg(w + q * 32 + h);
+        {  // the query's scales (B), replicated in every quadrant
+            const uint2 qs = __ldg(reinterpret_cast<const uint2*>(q_scales + (q * 32 + lane) * 8));
+            tmem_st4(lane_base + kColSfb, qs.x, 0u, 0u, 0u);
+            tmem_st4(lane_base + kColSfb + 4, qs.y, 0u, 0u, 0u);
+        }
+        auto stage_sf = [&](int i) -> bool {  // tile i's scales (A) into slot i % kTcSf
+            const int s = i % kTcStages, f = i % kTcSf;
+            if (!mbar_wait(&S.full[s], (i / kTcStages) & 1)) return false;
+            uint2 r4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r4[j] = *reinterpret_cast<const uint2*>(S.scales[s] + (lane + 32 * j) * 8);
+            tmem_st4(lane_base + kColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
+            tmem_st4(lane_base + kColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&S.sfa_ready[f]);
+            return true;
+        };
+        bool ok = stage_sf(0);
+        for (int i = 0; ok && i < ntiles; ++i) {
+            if (i + 1 < ntiles) ok = stage_sf(i + 1);
+            const int a = i % kTcAcc;
+            if (!ok || !mbar_wait(&S.acc_full[a], (i / kTcAcc) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[32];
+            tmem_ld32(lane_base + kColAcc + 32 * a, r);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&S.acc_empty[a]);
+            float x = 0.f;
+#pragma unroll
+            for (int h = 0; h < 32; ++h) x = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), x);
+            const int64_t t = t0 + i;
+            if (!GATHER) {
+                const int64_t pos = t * kTile + row;
+                float m = pos < n ? x : -INFINITY;
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                const int64_t b = pos >> 3;
+                if ((lane & 7) == 0 && b < nblk_vis) out[q * out_stride + b] = m;
+            } else {
+                const int64_t ci = t * 16 + (row >> 3);
+                if (ci < C) {
+                    const int32_t b = cq[ci];
+                    const bool v = b >= 0 && b < nblk_vis && 8 * int64_t(b) + (row & 7) < n;
+                    out[q * out_stride + 8 * ci + (row & 7)] = v ? x : -INFINITY;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            record(st, CSA2_ERR_TIMEOUT, 12, int32_t(q), 0);
+            S.abort_flag = 1;
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, kTcCols);
 }
 
 // ------------------------------------------------------------ selection
@@ -746,13 +688,44 @@ static csa2_status prepare_select_kernels() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
     if (done[dev]) return CSA2_OK;
     const int bytes = (kSelSmemKeys + kMaxPoolBlocks) * 4;
-    if (cudaFuncSetAttribute(scan_blockmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(sizeof(ScanSmem))) != cudaSuccess ||
+    if (cudaFuncSetAttribute(score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(TcScanSmem))) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(TcScanSmem))) != cudaSuccess ||
         cudaFuncSetAttribute(select_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return CSA2_ERR_CUDA;
     done[dev] = true;
     return CSA2_OK;
+}
+
+// CTAs per query for a tensor-core scorer launch: two resident CTAs per SM
+// over the whole batch, at most one per tile.
+static int64_t tc_ctas_per_query(int64_t n_q, int64_t tiles_max) {
+    int64_t cpq = 2 * kSMs / n_q;
+    return cpq < 1 ? 1 : (cpq > tiles_max ? tiles_max : cpq);
+}
+
+// Per-position scores of the candidate blocks, then their top-k (the pool
+// scoring of csa2_index_full and all of csa2_index_reindex).
+static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, const float* w, int64_t n_q,
+                             const uint8_t* k_codes, const uint8_t* k_scales, int64_t n_rows,
+                             const int64_t* kv_start, const int32_t* n_visible, int32_t max_visible,
+                             const int32_t* cand, int64_t cand_stride, int C, int topk, int32_t* out_topk,
+                             float* scores, int64_t score_stride, bool check_cand, Status* st, cudaStream_t s) {
+    const int64_t cpq = tc_ctas_per_query(n_q, (C + 15) / 16);
+    const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
+    timer_begin(K_POOL_SCORE, s);
+    score_tc_kernel<true><<<grid, kTcThreads, sizeof(TcScanSmem), s>>>(
+        q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand, cand_stride, C,
+        scores, score_stride, int(cpq), check_cand, st);
+    timer_end(K_POOL_SCORE, s);
+    const int cap_t = sel_cap(8 * int64_t(C));
+    timer_begin(K_SELECT_TOPK, s);
+    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + C) * 4, s>>>(
+        scores, score_stride, cand, cand_stride, C, kv_start, n_visible, max_visible, n_rows, topk, out_topk, topk,
+        cap_t);
+    timer_end(K_SELECT_TOPK, s);
 }
 
 }  // namespace csa2
@@ -781,15 +754,12 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
     float* scores = reinterpret_cast<float*>(base + L.scores);
     const int C = pool_blocks > topk ? pool_blocks : topk;
     if (max_visible > 0) {
-        // one CTA per SM: split each query's tiles over kSMs / n_q CTAs
-        const int64_t tiles_max = ceil_div<int64_t>(max_visible, kTile);
-        int64_t cpq = kSMs / n_q;
-        cpq = cpq < 1 ? 1 : (cpq > tiles_max ? tiles_max : cpq);
+        const int64_t cpq = tc_ctas_per_query(n_q, ceil_div<int64_t>(max_visible, kTile));
         const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
         timer_begin(K_SCAN, s);
-        scan_blockmax_kernel<<<grid, kScanThreads, sizeof(ScanSmem), s>>>(
-            q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, blockmax,
-            L.nb_stride, int(cpq), st);
+        score_tc_kernel<false><<<grid, kTcThreads, sizeof(TcScanSmem), s>>>(
+            q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0, 0,
+            blockmax, L.nb_stride, int(cpq), false, st);
         timer_end(K_SCAN, s);
     }
     const int cap_b = sel_cap(L.nb_stride);
@@ -810,19 +780,8 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         cand = wide;
         cand_stride = topk;
     }
-    dim3 pgrid(unsigned(ceil_div(C, kPoolBlocksPerCta)), unsigned(n_q));
-    timer_begin(K_POOL_SCORE, s);
-    pool_score_kernel<<<pgrid, kPoolWarps * 32, 0, s>>>(q_codes, q_scales, w, k_codes, k_scales, n_rows,
-                                                        kv_start, n_visible, max_visible, cand,
-                                                        cand_stride, C, scores, L.score_stride, st,
-                                                        false);
-    timer_end(K_POOL_SCORE, s);
-    const int cap_t = sel_cap(8 * int64_t(C));
-    timer_begin(K_SELECT_TOPK, s);
-    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + C) * 4, s>>>(
-        scores, L.score_stride, cand, cand_stride, C, kv_start, n_visible, max_visible, n_rows, topk,
-        out_topk, topk, cap_t);
-    timer_end(K_SELECT_TOPK, s);
+    launch_pool_topk(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand,
+                     cand_stride, C, topk, out_topk, scores, L.score_stride, false, st, s);
     return launch_status();
 }
 
@@ -845,19 +804,8 @@ extern "C" csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t*
     char* base = static_cast<char*>(ws);
     Status* st = reinterpret_cast<Status*>(base);
     float* scores = reinterpret_cast<float*>(base + L.scores);
-    dim3 pgrid(unsigned(ceil_div(pool_blocks, kPoolBlocksPerCta)), unsigned(n_q));
-    timer_begin(K_POOL_SCORE, s);
-    pool_score_kernel<<<pgrid, kPoolWarps * 32, 0, s>>>(q_codes, q_scales, w, k_codes, k_scales, n_rows,
-                                                        kv_start, n_visible, max_visible, pool,
-                                                        pool_blocks, pool_blocks, scores,
-                                                        L.score_stride, st, true);
-    timer_end(K_POOL_SCORE, s);
-    const int cap_t = sel_cap(8 * int64_t(pool_blocks));
-    timer_begin(K_SELECT_TOPK, s);
-    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + pool_blocks) * 4, s>>>(
-        scores, L.score_stride, pool, pool_blocks, pool_blocks, kv_start, n_visible, max_visible,
-        n_rows, topk, out_topk, topk, cap_t);
-    timer_end(K_SELECT_TOPK, s);
+    launch_pool_topk(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, pool,
+                     pool_blocks, pool_blocks, topk, out_topk, scores, L.score_stride, true, st, s);
     return launch_status();
 }
 
@@ -899,17 +847,7 @@ extern "C" csa2_status csa2_index_reindex_noalloc(const uint8_t* q_codes, const 
     const int64_t stride = 8 * int64_t(pool_blocks);
     Status* st = reinterpret_cast<Status*>(status);
     cudaStream_t s = cudaStream_t(stream);
-    dim3 pgrid(unsigned(ceil_div(pool_blocks, kPoolBlocksPerCta)), unsigned(n_q));
-    timer_begin(K_POOL_SCORE, s);
-    pool_score_kernel<<<pgrid, kPoolWarps * 32, 0, s>>>(q_codes, q_scales, w, k_codes, k_scales, n_rows,
-                                                        kv_start, n_visible, max_visible, pool,
-                                                        pool_blocks, pool_blocks, scores, stride, st, true);
-    timer_end(K_POOL_SCORE, s);
-    const int cap_t = sel_cap(stride);
-    timer_begin(K_SELECT_TOPK, s);
-    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + pool_blocks) * 4, s>>>(
-        scores, stride, pool, pool_blocks, pool_blocks, kv_start, n_visible, max_visible, n_rows, topk,
-        out_topk, topk, cap_t);
-    timer_end(K_SELECT_TOPK, s);
+    launch_pool_topk(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, pool,
+                     pool_blocks, pool_blocks, topk, out_topk, scores, stride, true, st, s);
     return launch_status();
 }
