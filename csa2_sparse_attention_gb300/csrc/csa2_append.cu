@@ -22,6 +22,8 @@ namespace csa2 {
 // The buffer holds the rows twice: as float2 (fast path) and then as double2
 // (exact fallback near rounding ties).
 __global__ void rope_table_kernel(float theta, int dim, int n_hi, float2* t32, double2* t64) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int half = dim / 2;
     const int64_t total = int64_t(n_hi + 1024) * half;
     for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < total;
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(
     uint8_t* __restrict__ scales, Status* st) {
     constexpr int TPR = DIM / 16;
     constexpr int RPB = 256 / TPR;  // rows per block per iteration
+    grid_dep_wait();
+    grid_dep_launch();
     const int g = threadIdx.x % TPR;
     for (int64_t i = blockIdx.x * int64_t(RPB) + threadIdx.x / TPR; i < n;
          i += int64_t(gridDim.x) * RPB) {
@@ -201,6 +205,8 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(
     uint8_t* __restrict__ dst, Status* st) {
     constexpr int TPR = DIM / 16;
     constexpr int RPB = 256 / TPR;
+    grid_dep_wait();
+    grid_dep_launch();
     const int g = threadIdx.x % TPR;
     for (int64_t i = blockIdx.x * int64_t(RPB) + threadIdx.x / TPR; i < n;
          i += int64_t(gridDim.x) * RPB) {
@@ -248,7 +254,7 @@ extern "C" csa2_status csa2_rope_table_init(float theta, int dim, int64_t max_po
     float2* t32 = static_cast<float2*>(table);
     double2* t64 = reinterpret_cast<double2*>(t32 + int64_t(n_hi + 1024) * (dim / 2));
     timer_begin(K_ROPE_TABLE, cudaStream_t(stream));
-    rope_table_kernel<<<256, 256, 0, cudaStream_t(stream)>>>(theta, dim, n_hi, t32, t64);
+    launch(rope_table_kernel, 256, 256, 0, cudaStream_t(stream), 1, theta, dim, n_hi, t32, t64);
     timer_end(K_ROPE_TABLE, cudaStream_t(stream));
     return launch_status();
 }
@@ -273,9 +279,9 @@ extern "C" csa2_status csa2_quantize_append(const void* x_bf16, int64_t n, int d
         if (layout != CSA2_LAYOUT_ROWS || pos != nullptr) return CSA2_ERR_UNSUPPORTED;
         timer_begin(K_QUANT_FP8, s);
         if (dim == 512)
-            quantize_fp8_kernel<512><<<grid_for(n, 8), 256, 0, s>>>(x, n, dst_row, n_rows, dst_codes, st);
+            launch(quantize_fp8_kernel<512>, grid_for(n, 8), 256, 0, s, 1, x, n, dst_row, n_rows, dst_codes, st);
         else
-            quantize_fp8_kernel<128><<<grid_for(n, 32), 256, 0, s>>>(x, n, dst_row, n_rows, dst_codes, st);
+            launch(quantize_fp8_kernel<128>, grid_for(n, 32), 256, 0, s, 1, x, n, dst_row, n_rows, dst_codes, st);
         timer_end(K_QUANT_FP8, s);
         return launch_status();
     }
@@ -292,13 +298,13 @@ extern "C" csa2_status csa2_quantize_append(const void* x_bf16, int64_t n, int d
     }
     timer_begin(K_QUANT_FP4, s);
     if (dim == 512)
-        quantize_fp4_kernel<512, false><<<grid_for(n, 8), 256, 0, s>>>(
+        launch(quantize_fp4_kernel<512, false>, grid_for(n, 8), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     else if (layout == CSA2_LAYOUT_BLOCK8)
-        quantize_fp4_kernel<128, true><<<grid_for(n, 32), 256, 0, s>>>(
+        launch(quantize_fp4_kernel<128, true>, grid_for(n, 32), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     else
-        quantize_fp4_kernel<128, false><<<grid_for(n, 32), 256, 0, s>>>(
+        launch(quantize_fp4_kernel<128, false>, grid_for(n, 32), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     timer_end(K_QUANT_FP4, s);
     return launch_status();

@@ -101,21 +101,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const int split = blockIdx.x;
     const int64_t q = blockIdx.y;
 
-    // the query's row range and this thread's two top-k entries, first
-    const int64_t ks = kv_start[q];
-    const int32_t nv = n_visible[q];
-    const int pre_ge = split * kTcE + (tid & (kTcE - 1));  // this thread's entry (both items)
-    const int32_t pre = pre_ge < k ? topk[q * k + pre_ge] : -1;
     if (tid == 0) {
         mbar_init(&S.bar, 1);
         mbar_init_fence();
-    }
-    if (warp == 0) tmem_alloc(&S.tmem, kTcCols);
-    // Q (bf16 [64][512]) into the canonical K-major layout, asynchronously
-    const uint16_t* qsrc = qg + q * (kH * kD);
-    for (int i = tid; i < kH * kD / 8; i += kAttnThreads) {
-        const int h = i >> 6, c = i & 63;
-        cp_async16(smem_addr(S.r0 + row512(h, c)), qsrc + h * kD + c * 8);
     }
     {  // tables: E2M1 pair -> bf16x2, E4M3 -> bf16 (exact)
         const int b = tid;
@@ -124,6 +112,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         const float hi = (b & 128 ? -1.f : 1.f) * e2m1[(b >> 4) & 7];
         S.lut4[b] = uint32_t(bf16_bits(lo)) | (uint32_t(bf16_bits(hi)) << 16);
         S.lut8[b] = bf16_bits(e4m3_value(uint32_t(b)));
+    }
+    grid_dep_wait();
+    grid_dep_launch();
+    // the query's row range and this thread's two top-k entries, first
+    const int64_t ks = kv_start[q];
+    const int32_t nv = n_visible[q];
+    const int pre_ge = split * kTcE + (tid & (kTcE - 1));  // this thread's entry (both items)
+    const int32_t pre = pre_ge < k ? topk[q * k + pre_ge] : -1;
+    if (warp == 0) tmem_alloc(&S.tmem, kTcCols);
+    // Q (bf16 [64][512]) into the canonical K-major layout, asynchronously
+    const uint16_t* qsrc = qg + q * (kH * kD);
+    for (int i = tid; i < kH * kD / 8; i += kAttnThreads) {
+        const int h = i >> 6, c = i & 63;
+        cp_async16(smem_addr(S.r0 + row512(h, c)), qsrc + h * kD + c * 8);
     }
     int32_t n = 0;  // per-query validity, reported once per query
     {
@@ -415,6 +417,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     const int64_t q = blockIdx.x;
     const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
     const int lane = lane_id();
+    grid_dep_wait();
+    grid_dep_launch();
     // lane s < splits holds split s's (m, l); at most 128 splits
     float M = -INFINITY, ms[4], ls[4];
 #pragma unroll
@@ -567,35 +571,25 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     if (e != CSA2_OK) return e;
     // one cluster per query when every cluster of the launch is resident at once
     const bool cluster = L.splits <= 8 && n_q <= max_clusters;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q), 1);
-    cfg.blockDim = dim3(kAttnThreads, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(AttnTcSmem);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    if (cluster) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(L.splits);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
+    const dim3 grid(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q), 1);
     timer_begin(K_ATTN_SPLIT, s);
     const cudaError_t le =
-        cluster ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, q, kv_codes, kv_scales, n_rows, kv_start, n_visible,
-                                     topk, k, swa, sn, window, sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st)
-                : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, q, kv_codes, kv_scales, n_rows, kv_start,
-                                     n_visible, topk, k, swa, sn, window, sm_scale, part_o, part_ml, L.splits, out,
-                                     f32, out_lse, st);
+        cluster ? launch(attn_tc_kernel<true>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
+                         kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, sm_scale, part_o,
+                         part_ml, L.splits, out, f32, out_lse, st)
+                : launch(attn_tc_kernel<false>, grid, kAttnThreads, sizeof(AttnTcSmem), s, 1, q, kv_codes,
+                         kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, sm_scale, part_o, part_ml,
+                         L.splits, out, f32, out_lse, st);
     timer_end(K_ATTN_SPLIT, s);
     if (le != cudaSuccess) return CSA2_ERR_CUDA;
     if (cluster) return launch_status();
     timer_begin(K_ATTN_MERGE, s);
     if (f32)
-        attn_merge_kernel<true><<<dim3(unsigned(n_q), kH / 8), 256, 0, s>>>(part_o, part_ml, L.splits, out, out_lse);
+        launch(attn_merge_kernel<true>, dim3(unsigned(n_q), kH / 8), 256, 0, s, 1, part_o, part_ml, L.splits, out,
+               out_lse);
     else
-        attn_merge_kernel<false><<<dim3(unsigned(n_q), kH / 8), 256, 0, s>>>(part_o, part_ml, L.splits, out, out_lse);
+        launch(attn_merge_kernel<false>, dim3(unsigned(n_q), kH / 8), 256, 0, s, 1, part_o, part_ml, L.splits, out,
+               out_lse);
     timer_end(K_ATTN_MERGE, s);
     return launch_status();
 }

@@ -125,6 +125,18 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization, so it may become resident while
+// the previous kernel of the stream is still running.  grid_dep_wait()
+// returns once that kernel has completed and its memory is visible (at once
+// when there is none); nothing written by earlier work in the stream may be
+// read, and nothing may be written to global memory, before it.
+// grid_dep_launch() then lets the next kernel start its own launch.  A kernel
+// allocates TMEM only after grid_dep_wait(), so it never waits on columns
+// held by its predecessor.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <typename T>
 __host__ __device__ constexpr T ceil_div(T a, T b) { return (a + b - 1) / b; }
 
@@ -134,4 +146,29 @@ __host__ __device__ constexpr T ceil_div(T a, T b) { return (a + b - 1) / b; }
 namespace csa2 {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 csa2_status launch_status();  // maps cudaGetLastError to a csa2_status
+
+// Launches `kernel` on `s` with programmatic stream serialization (see
+// grid_dep_wait) and, when cluster > 1, clusters of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, unsigned cluster,
+                   Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 }  // namespace csa2

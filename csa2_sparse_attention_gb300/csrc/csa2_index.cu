@@ -61,11 +61,15 @@ constexpr int kTcAcc = 4;            // accumulator stages (32 TMEM columns each
 constexpr int kTcSf = 4;             // scale-factor slots (8 columns each)
 constexpr uint32_t kTcCols = 256;
 constexpr uint32_t kColAcc = 0, kColSfa = 128, kColSfb = 160;
+constexpr int kTcSfLead = 3;         // tiles whose scales are staged ahead (< kTcSf)
+constexpr int kTcMaxCandPerCta = 4096;
+static_assert(kTcMaxCandPerCta >= kMaxPoolBlocks, "a CTA stages at most all candidate blocks");
 
 struct TcScanSmem {
     uint8_t codes[kTcStages][kTile * 64];
     uint8_t scales[kTcStages][kTile * 8];
     uint8_t qcodes[32 * 64];          // the query's 32 heads, BLOCK8 = canonical K-major
+    int32_t cand[kTcMaxCandPerCta];   // this CTA's candidate blocks (pool scoring)
     uint64_t full[kTcStages], empty[kTcStages];
     uint64_t sfa_ready[kTcSf];
     uint64_t acc_full[kTcAcc], acc_empty[kTcAcc];
@@ -85,6 +89,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
     const int64_t q = blockIdx.y;
+    grid_dep_wait();
+    grid_dep_launch();
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, GATHER ? nullptr : st,
                                       !GATHER && blockIdx.x == 0 && threadIdx.x == 0);
     const int64_t nblk_vis = (int64_t(n) + 7) >> 3;
@@ -118,6 +124,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         mbar_init_fence();
     }
     if (warp == 1) tmem_alloc(&S.tmem, kTcCols);
+    if (GATHER) {  // this CTA's candidate ids, once, by every thread
+        const int64_t c_lo = t0 * 16, c_hi = t1 * 16 < C ? t1 * 16 : C;
+        for (int64_t ci = c_lo + threadIdx.x; ci < c_hi; ci += blockDim.x) S.cand[ci - c_lo] = cq[ci];
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -147,7 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int64_t ci = t * 16 + j;
-                        bl[j] = ci < C ? cq[ci] : -1;
+                        bl[j] = ci < C ? S.cand[ci - t0 * 16] : -1;
                         if (bl[j] >= 0 && bl[j] < nblk_vis) bytes += 512 + 64;
                         else if (check_cand && (bl[j] < -1 || bl[j] >= nblk_vis))
                             record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), bl[j]);
@@ -212,9 +222,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
             mbar_arrive(&S.sfa_ready[f]);
             return true;
         };
-        bool ok = stage_sf(0);
+        bool ok = true;
+        for (int i = 0; ok && i < kTcSfLead && i < ntiles; ++i) ok = stage_sf(i);
         for (int i = 0; ok && i < ntiles; ++i) {
-            if (i + 1 < ntiles) ok = stage_sf(i + 1);
+            // tile i + lead reuses the slot of tile i + lead - kTcSf, whose MMA
+            // finished before tile i - 1's accumulator was read
+            if (i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
             const int a = i % kTcAcc;
             if (!ok || !mbar_wait(&S.acc_full[a], (i / kTcAcc) & 1)) {
                 ok = false;
@@ -241,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
             } else {
                 const int64_t ci = t * 16 + (row >> 3);
                 if (ci < C) {
-                    const int32_t b = cq[ci];
+                    const int32_t b = S.cand[ci - t0 * 16];
                     const bool v = b >= 0 && b < nblk_vis && 8 * int64_t(b) + (row & 7) < n;
                     out[q * out_stride + 8 * ci + (row & 7)] = v ? x : -INFINITY;
                 }
@@ -594,6 +607,8 @@ __global__ void __launch_bounds__(kSelThreads) select_blocks_kernel(
     extern __shared__ uint32_t smem_keys[];
     __shared__ SelShared sm;
     const int64_t q = blockIdx.x;
+    grid_dep_wait();
+    grid_dep_launch();
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
     const int nb = (n + 7) >> 3;
     const float* v = blockmax + q * nb_stride;
@@ -626,6 +641,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     int32_t* cblk = reinterpret_cast<int32_t*>(smem_dyn);
     uint32_t* keys = smem_dyn + C;
     const int64_t q = blockIdx.x;
+    grid_dep_wait();
+    grid_dep_launch();
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
     const int32_t* cq = cand + q * cand_stride;
     const int nb = (n + 7) >> 3;
@@ -716,13 +733,13 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
     const int64_t cpq = tc_ctas_per_query(n_q, (C + 15) / 16);
     const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
     timer_begin(K_POOL_SCORE, s);
-    score_tc_kernel<true><<<grid, kTcThreads, sizeof(TcScanSmem), s>>>(
+    launch(score_tc_kernel<true>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
         q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand, cand_stride, C,
         scores, score_stride, int(cpq), check_cand, st);
     timer_end(K_POOL_SCORE, s);
     const int cap_t = sel_cap(8 * int64_t(C));
     timer_begin(K_SELECT_TOPK, s);
-    select_topk_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_t + C) * 4, s>>>(
+    launch(select_topk_kernel, unsigned(n_q), kSelThreads, size_t(cap_t + C) * 4, s, 1,
         scores, score_stride, cand, cand_stride, C, kv_start, n_visible, max_visible, n_rows, topk, out_topk, topk,
         cap_t);
     timer_end(K_SELECT_TOPK, s);
@@ -757,14 +774,14 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         const int64_t cpq = tc_ctas_per_query(n_q, ceil_div<int64_t>(max_visible, kTile));
         const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
         timer_begin(K_SCAN, s);
-        score_tc_kernel<false><<<grid, kTcThreads, sizeof(TcScanSmem), s>>>(
+        launch(score_tc_kernel<false>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0, 0,
             blockmax, L.nb_stride, int(cpq), false, st);
         timer_end(K_SCAN, s);
     }
     const int cap_b = sel_cap(L.nb_stride);
     timer_begin(K_SELECT_BLOCKS, s);
-    select_blocks_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_b) * 4, s>>>(
+    launch(select_blocks_kernel, unsigned(n_q), kSelThreads, size_t(cap_b) * 4, s, 1,
         blockmax, L.nb_stride, kv_start, n_visible, max_visible, n_rows, pool_blocks, out_pool,
         pool_blocks, cap_b);
     timer_end(K_SELECT_BLOCKS, s);
@@ -774,7 +791,7 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         // the top-k positions lie in the top-max(P, K) blocks
         int32_t* wide = reinterpret_cast<int32_t*>(base + L.cand);
         timer_begin(K_SELECT_BLOCKS, s);
-        select_blocks_kernel<<<unsigned(n_q), kSelThreads, size_t(cap_b) * 4, s>>>(
+        launch(select_blocks_kernel, unsigned(n_q), kSelThreads, size_t(cap_b) * 4, s, 1,
             blockmax, L.nb_stride, kv_start, n_visible, max_visible, n_rows, topk, wide, topk, cap_b);
         timer_end(K_SELECT_BLOCKS, s);
         cand = wide;
