@@ -47,11 +47,9 @@ constexpr uint32_t kTcCols = 512;  // TMEM columns: S^T (64) + O^T (4 x 64)
 struct AttnTcSmem {
     uint8_t r0[64 * 1024];         // Q bf16 (B of S^T); then S fp32 [64][128] + P hi/lo f16
     uint8_t c[kTcE * 1024];        // C [128 entries][512] bf16, then f16
-    uint32_t lut4[256];            // E2M1 pair -> bf16x2 (unscaled)
-    uint16_t lut8[256];            // E4M3 byte -> bf16
+    uint32_t lut4[256 * 32];       // E2M1 pair -> bf16x2 (unscaled); byte b, lane l at [b * 32 + l]
     int ok[kTcE];                  // entry valid
     float ml[kH][2];               // this split's (m, l) per head
-    float wts[kH][8];              // cluster merge weights a_s / L per head and split
     uint64_t bar;                  // MMA completion (phase 0: S, phase 1: O)
     uint32_t tmem;
 };
@@ -84,6 +82,63 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Two E4M3 bytes, one in the low byte of each 16-bit half of x, as bf16x2
+// (exact).  The sign goes to bit 15 and the 7 exponent/mantissa bits to bits
+// 4..10, which is the bf16 pattern of the value times 2^-120 (E4M3 and bf16
+// subnormals line up); one multiply by 2^120 restores it.  The NaN codes
+// (0x7F, 0xFF), which the FP8 append never writes, read as +-480.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t x) {
+    const uint32_t sgn = x & 0x00800080u;
+    return bf16x2_mul((x + sgn * 15u) << 4, 0x7B807B80u);
+}
+
+// One quarter (128 channels) of an FP4 latent row: 4 x 16 bytes of E2M1
+// codes and 8 E4M3 scales, as bf16 into row e of C.  `lut` is the calling
+// lane's column of the pair table, so the 32 lanes of a warp read 32
+// distinct banks whatever the codes.
+__device__ __forceinline__ void fp4_quarter_to_c(const uint4 (&v)[4], uint2 sc, const uint32_t* lut, uint8_t* c,
+                                                 int e, int qq) {
+    const uint32_t scw[2] = {sc.x, sc.y};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // scale groups 2j, 2j+1 of this quarter
+            const uint32_t sb = (scw[(2 * j + h) >> 2] >> (8 * ((2 * j + h) & 3))) & 0xFF;
+            const uint32_t s16 = bf16_bits(e4m3_value(sb));
+            const uint32_t s2 = s16 | (s16 << 16);
+            uint32_t outw[8];
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const uint32_t w = wv[2 * h + m];
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) outw[4 * m + bb] = bf16x2_mul(lut[((w >> (8 * bb)) & 0xFF) * 32], s2);
+            }
+            const int chunk = qq * 16 + 4 * j + 2 * h;
+            *reinterpret_cast<uint4*>(c + row512(e, chunk)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            *reinterpret_cast<uint4*>(c + row512(e, chunk + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+        }
+    }
+}
+
+// One quarter (128 channels) of an FP8 window row (8 x 16 bytes) as bf16
+// into row e of C.
+__device__ __forceinline__ void fp8_quarter_to_c(const uint4 (&v)[8], uint8_t* c, int e, int qq) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        uint32_t outw[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            outw[2 * m] = e4m3x2_to_bf16x2(__byte_perm(wv[m], 0, 0x4140));
+            outw[2 * m + 1] = e4m3x2_to_bf16x2(__byte_perm(wv[m], 0, 0x4342));
+        }
+        const int chunk = qq * 16 + 2 * j;
+        *reinterpret_cast<uint4*>(c + row512(e, chunk)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        *reinterpret_cast<uint4*>(c + row512(e, chunk + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    }
+}
+
 // grid (splits, n_q), 256 threads, one CTA per SM.  The split's unnormalized
 // partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [64][512]) and (m_s, l_s) per
 // head go to the workspace, or (CLUSTER) are merged across the cluster.
@@ -105,20 +160,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         mbar_init(&S.bar, 1);
         mbar_init_fence();
     }
-    {  // tables: E2M1 pair -> bf16x2, E4M3 -> bf16 (exact)
-        const int b = tid;
-        const float e2m1[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
-        const float lo = (b & 8 ? -1.f : 1.f) * e2m1[b & 7];
-        const float hi = (b & 128 ? -1.f : 1.f) * e2m1[(b >> 4) & 7];
-        S.lut4[b] = uint32_t(bf16_bits(lo)) | (uint32_t(bf16_bits(hi)) << 16);
-        S.lut8[b] = bf16_bits(e4m3_value(uint32_t(b)));
+    {  // E2M1 pair -> bf16x2 (exact), one copy per lane
+        auto e2m1 = [](int c) {  // magnitude bits: 2 exponent (bias 1), 1 mantissa
+            const int ex = (c >> 1) & 3, m = c & 1;
+            const float v = ex == 0 ? 0.5f * float(m) : ldexpf(1.f + 0.5f * float(m), ex - 1);
+            return (c & 8) ? -v : v;
+        };
+        for (int i = tid; i < 256 * 32; i += kAttnThreads) {
+            const int b = i >> 5;
+            S.lut4[i] = uint32_t(bf16_bits(e2m1(b & 15))) | (uint32_t(bf16_bits(e2m1(b >> 4))) << 16);
+        }
     }
     grid_dep_wait();
     grid_dep_launch();
     // the query's row range and this thread's two top-k entries, first
     const int64_t ks = kv_start[q];
     const int32_t nv = n_visible[q];
-    const int pre_ge = split * kTcE + (tid & (kTcE - 1));  // this thread's entry (both items)
+    // the sequence (top-k entries, then window entries) in groups of 32:
+    // split s takes groups s, s + splits, s + 2 splits, s + 3 splits, so the
+    // splits get about the same mix and each warp one kind of entry
+    const int pre_ge = (((tid & (kTcE - 1)) >> 5) * splits + split) * 32 + (tid & 31);  // this thread's entry
     const int32_t pre = pre_ge < k ? topk[q * k + pre_ge] : -1;
     if (warp == 0) tmem_alloc(&S.tmem, kTcCols);
     // Q (bf16 [64][512]) into the canonical K-major layout, asynchronously
@@ -139,96 +200,81 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         }
     }
     const int nw = n < window ? n : window;
-    __syncthreads();  // tables ready
-
-    // gather + dequantize: item -> (entry e = item % 128, quarter qq = item / 128);
-    // consecutive lanes take consecutive entries, so each 16-byte store of a
-    // warp phase lands on distinct banks
-    for (int item = tid; item < kTcE * 4; item += kAttnThreads) {
-        const int e = item & (kTcE - 1), qq = item >> 7;
-        const int ge = split * kTcE + e;
+    __syncthreads();  // pair table ready
+    // gather + dequantize: thread -> entry e = tid % 128 and channel quarters
+    // qa, qa + 2 (qa = tid / 128); consecutive lanes take consecutive entries,
+    // so each 16-byte store of a warp phase lands on distinct banks.  All
+    // loads of a thread are issued before its first conversion.
+    {
+        const int e = tid & (kTcE - 1), qa = tid >> 7;
+        const int ge = pre_ge;
+        const uint32_t* lut = S.lut4 + lane;
         bool ok = false;
         if (ge < k) {
             const int32_t p = pre;
             if (p >= 0 && p < n) {
                 ok = true;
                 const int64_t row = ks + p;
-                const uint4* src = reinterpret_cast<const uint4*>(kv_codes + row * 256 + qq * 64);
-                const uint2 sc = __ldg(reinterpret_cast<const uint2*>(kv_scales + row * 32 + qq * 8));
-                uint4 v[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) v[j] = __ldg(src + j);
-                const uint32_t scw[2] = {sc.x, sc.y};
+                const uint4* src = reinterpret_cast<const uint4*>(kv_codes + row * 256);
+                const uint2* ssrc = reinterpret_cast<const uint2*>(kv_scales + row * 32);
+                uint4 v0[4], v1[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {  // groups 2j, 2j+1 of this quarter
-                        const uint32_t sb = (scw[(2 * j + h) >> 2] >> (8 * ((2 * j + h) & 3))) & 0xFF;
-                        const uint32_t s16 = S.lut8[sb];
-                        const uint32_t s2 = s16 | (s16 << 16);
-                        uint32_t outw[8];
-#pragma unroll
-                        for (int m = 0; m < 2; ++m) {
-                            const uint32_t w = wv[2 * h + m];
-#pragma unroll
-                            for (int bb = 0; bb < 4; ++bb)
-                                outw[4 * m + bb] = bf16x2_mul(S.lut4[(w >> (8 * bb)) & 0xFF], s2);
-                        }
-                        const int chunk = qq * 16 + 4 * j + 2 * h;
-                        *reinterpret_cast<uint4*>(S.c + row512(e, chunk)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-                        *reinterpret_cast<uint4*>(S.c + row512(e, chunk + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-                    }
+                    v0[j] = __ldg(src + qa * 4 + j);
+                    v1[j] = __ldg(src + (qa + 2) * 4 + j);
                 }
+                const uint2 s0 = __ldg(ssrc + qa), s1 = __ldg(ssrc + qa + 2);
+                fp4_quarter_to_c(v0, s0, lut, S.c, e, qa);
+                fp4_quarter_to_c(v1, s1, lut, S.c, e, qa + 2);
             } else if (p < -1 || p >= n) {
-                if (qq == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_TOPK, int32_t(q), p);
+                if (qa == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_TOPK, int32_t(q), p);
             }
         } else if (ge - k < nw) {
             ok = true;
             const int64_t pos = int64_t(n - nw) + (ge - k);
             const int64_t slot = pos % window;
-            uint8_t* ring = swa + (q * window + slot) * kD + qq * 128;
-            uint4 v[8];
+            uint8_t* ring = swa + (q * window + slot) * kD;
             if (swa_new != nullptr && pos == n - 1) {
                 // current token: E4M3 of its bf16 latent, stored to the ring and used here
-                const uint4* src = reinterpret_cast<const uint4*>(swa_new + q * kD + qq * 128);
+#pragma unroll 1
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int qq = qa + 2 * h2;
+                    const uint4* src = reinterpret_cast<const uint4*>(swa_new + q * kD + qq * 128);
+                    uint4 v[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 a = __ldg(src + 2 * j), b = __ldg(src + 2 * j + 1);
-                    const uint32_t w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                    uint32_t o4[4];
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 a = __ldg(src + 2 * j), b = __ldg(src + 2 * j + 1);
+                        const uint32_t w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                        uint32_t o4[4];
 #pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        o4[m] = e4m3x2_rn_sat(bf16_lo(w8[2 * m]), bf16_hi(w8[2 * m])) |
-                                (e4m3x2_rn_sat(bf16_lo(w8[2 * m + 1]), bf16_hi(w8[2 * m + 1])) << 16);
-                    v[j] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-                    reinterpret_cast<uint4*>(ring)[j] = v[j];
+                        for (int m = 0; m < 4; ++m)
+                            o4[m] = e4m3x2_rn_sat(bf16_lo(w8[2 * m]), bf16_hi(w8[2 * m])) |
+                                    (e4m3x2_rn_sat(bf16_lo(w8[2 * m + 1]), bf16_hi(w8[2 * m + 1])) << 16);
+                        v[j] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                        reinterpret_cast<uint4*>(ring + qq * 128)[j] = v[j];
+                    }
+                    fp8_quarter_to_c(v, S.c, e, qq);
                 }
             } else {
-                const uint4* src = reinterpret_cast<const uint4*>(ring);
+                const uint4* src0 = reinterpret_cast<const uint4*>(ring + qa * 128);
+                const uint4* src1 = reinterpret_cast<const uint4*>(ring + (qa + 2) * 128);
+                uint4 v0[8], v1[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = src[j];
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                uint32_t outw[8];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t w = wv[m];
-                    outw[2 * m] = uint32_t(S.lut8[w & 0xFF]) | (uint32_t(S.lut8[(w >> 8) & 0xFF]) << 16);
-                    outw[2 * m + 1] = uint32_t(S.lut8[(w >> 16) & 0xFF]) | (uint32_t(S.lut8[w >> 24]) << 16);
+                for (int j = 0; j < 8; ++j) {
+                    v0[j] = src0[j];
+                    v1[j] = src1[j];
                 }
-                const int chunk = qq * 16 + 2 * j;
-                *reinterpret_cast<uint4*>(S.c + row512(e, chunk)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-                *reinterpret_cast<uint4*>(S.c + row512(e, chunk + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+                fp8_quarter_to_c(v0, S.c, e, qa);
+                fp8_quarter_to_c(v1, S.c, e, qa + 2);
             }
         }
         if (!ok) {
-            for (int c = qq * 16; c < qq * 16 + 16; ++c)
-                *reinterpret_cast<uint4*>(S.c + row512(e, c)) = make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2)
+                for (int c = (qa + 2 * h2) * 16; c < (qa + 2 * h2) * 16 + 16; ++c)
+                    *reinterpret_cast<uint4*>(S.c + row512(e, c)) = make_uint4(0, 0, 0, 0);
         }
-        if (qq == 0) S.ok[e] = ok;
+        if (qa == 0) S.ok[e] = ok;
     }
     cp_async_wait_all();
     fence_async_smem();
@@ -343,6 +389,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();  // every partial and (m, l) of the query is visible
         const int rank = int(cluster.block_rank());
+        float(*wts)[8] = reinterpret_cast<float(*)[8]>(S.r0);  // P is consumed: merge weights a_s / L
         if (tid < kH) {  // merge weights of head tid
             float mp[8], lp[8], M = -INFINITY;
 #pragma unroll
@@ -364,7 +411,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             }
             const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-            for (int p = 0; p < 8; ++p) S.wts[tid][p] = a[p] * inv;
+            for (int p = 0; p < 8; ++p) wts[tid][p] = a[p] * inv;
             if (rank == 0 && out_lse) out_lse[q * kH + tid] = L > 0.f ? M + logf(L) : -INFINITY;
         }
         __syncthreads();
@@ -385,7 +432,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
-                const float wgt = p < splits ? S.wts[h][p] : 0.f;
+                const float wgt = p < splits ? wts[h][p] : 0.f;
                 o.x = fmaf(wgt, v[p].x, o.x);
                 o.y = fmaf(wgt, v[p].y, o.y);
                 o.z = fmaf(wgt, v[p].z, o.z);

@@ -120,3 +120,44 @@ def test_attention_bf16_output_within_its_rounding():
         o = bf16_to_f64(g.out[li][0])
         err = np.abs(o - o_ref)
         assert np.all(err <= 2.0 ** -8 * np.abs(o_ref) + 1e-5 * np.abs(o_ref).max(axis=-1, keepdims=True))
+
+
+def test_attention_subnormal_window_bytes_and_scales():
+    """Window bytes that are all E4M3 subnormals (|x| <= 7 * 2^-9) and FP4
+    rows whose scales are all subnormal: the output is made of those values
+    only, so a decode that flushed them to zero fails the relative check."""
+    from csa2_sparse_attention_gb300 import abi
+    rng = np.random.default_rng(12)
+    n_rows, B, K, Wn = 64, 3, 16, 128
+    codes = rng.integers(0, 256, (n_rows, 256)).astype(np.uint8)
+    scales = rng.integers(0x01, 0x08, (n_rows, 32)).astype(np.uint8)          # subnormal scales
+    sub = np.concatenate([np.arange(0x01, 0x08), np.arange(0x81, 0x88)]).astype(np.uint8)
+    swa = rng.choice(sub, (B, Wn, 512)).astype(np.uint8)                     # subnormal window
+    q = torch.randn((B, 64, 512), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    kv_start = np.array([0, 16, 32], dtype=np.int64)
+    n_vis = np.array([16, 16, 30], dtype=np.int32)
+    top = np.full((B, K), -1, dtype=np.int32)
+    top[1, :6] = [0, 2, 4, 6, 8, 10]     # query 0: window only; 1: both; 2: top-k only (window 0)
+    top[2, :16] = np.arange(16)
+    d = "cuda"
+    t = lambda a: torch.from_numpy(a).to(d)
+    out = torch.zeros((B, 64, 512), dtype=torch.float32, device=d)
+    lse = torch.zeros((B, 64), dtype=torch.float32, device=d)
+    qn = bf16_to_f64(q)
+    for window in (Wn, 0):
+        ws = torch.zeros(abi.csa2_workspace_bytes(abi.OP_SPARSE_ATTN, B, 16, 1, K), dtype=torch.uint8, device=d)
+        abi.csa2_sparse_attn(q.to(d), B, t(codes), t(scales), n_rows, t(kv_start), t(n_vis), t(top), K,
+                             t(swa), None, window, 1 / np.sqrt(512), out, abi.OUT_F32, lse, ws, ws.numel())
+        torch.cuda.synchronize()
+        assert abi.csa2_status_fetch(ws)[0] == 0
+        for b in range(B):
+            rows = codes[kv_start[b]:kv_start[b] + n_vis[b]]
+            sel, win = O.attention_inputs(top[b], O.unpack_codes(rows), scales[kv_start[b]:kv_start[b] + n_vis[b]],
+                                          swa[b], int(n_vis[b]), Wn)
+            if window == 0:
+                win = win[:0]
+            if sel.shape[0] + win.shape[0] == 0:
+                continue
+            o_ref, _ = O.sparse_attention(qn[b], sel, win)
+            assert np.abs(o_ref).max() < 2.0 ** -3 * 6  # built from subnormal-scale values only
+            check_attention(bf16_to_f64(out[b]), o_ref, f"subnormal b{b} window {window}")
