@@ -200,6 +200,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         }
     }
     const int nw = n < window ? n : window;
+    // the current token's window entry, when this call appends it: its
+    // position in this CTA (uniform over the CTA) or -1
+    int cur_e = -1;
+    if (swa_new != nullptr && nw > 0) {
+        const int cur_ge = k + nw - 1, grp = cur_ge >> 5;
+        if (grp % splits == split) cur_e = (grp / splits) * 32 + (cur_ge & 31);
+    }
+    if (cur_e >= 0) {  // E4M3 of its bf16 latent, two channels per thread: to the ring and into C
+        uint8_t* ring = swa + (q * window + int64_t(n - 1) % window) * kD;
+        const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid);
+        const uint32_t b2 = e4m3x2_rn_sat(bf16_lo(x), bf16_hi(x));
+        reinterpret_cast<uint16_t*>(ring)[tid] = static_cast<uint16_t>(b2);
+        *reinterpret_cast<uint32_t*>(S.c + row512(cur_e, tid >> 2) + (tid & 3) * 4) =
+            e4m3x2_to_bf16x2((b2 & 0xFFu) | ((b2 & 0xFF00u) << 8));
+    }
     __syncthreads();  // pair table ready
     // gather + dequantize: thread -> entry e = tid % 128 and channel quarters
     // qa, qa + 2 (qa = tid / 128); consecutive lanes take consecutive entries,
@@ -233,28 +248,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             ok = true;
             const int64_t pos = int64_t(n - nw) + (ge - k);
             const int64_t slot = pos % window;
-            uint8_t* ring = swa + (q * window + slot) * kD;
-            if (swa_new != nullptr && pos == n - 1) {
-                // current token: E4M3 of its bf16 latent, stored to the ring and used here
-#pragma unroll 1
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int qq = qa + 2 * h2;
-                    const uint4* src = reinterpret_cast<const uint4*>(swa_new + q * kD + qq * 128);
-                    uint4 v[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 a = __ldg(src + 2 * j), b = __ldg(src + 2 * j + 1);
-                        const uint32_t w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                        uint32_t o4[4];
-#pragma unroll
-                        for (int m = 0; m < 4; ++m)
-                            o4[m] = e4m3x2_rn_sat(bf16_lo(w8[2 * m]), bf16_hi(w8[2 * m])) |
-                                    (e4m3x2_rn_sat(bf16_lo(w8[2 * m + 1]), bf16_hi(w8[2 * m + 1])) << 16);
-                        v[j] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-                        reinterpret_cast<uint4*>(ring + qq * 128)[j] = v[j];
-                    }
-                    fp8_quarter_to_c(v, S.c, e, qq);
-                }
+            const uint8_t* ring = swa + (q * window + slot) * kD;
+            if (e == cur_e) {
+                // the current token: encoded and placed above
             } else {
                 const uint4* src0 = reinterpret_cast<const uint4*>(ring + qa * 128);
                 const uint4* src1 = reinterpret_cast<const uint4*>(ring + (qa + 2) * 128);
