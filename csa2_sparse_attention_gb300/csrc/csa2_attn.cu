@@ -8,20 +8,22 @@
 // before attention and the window KV stays FP8.
 //
 // Split-K over entries on the 5th-generation tensor cores.  CTA (split,
-// query) takes 128 entries: it gathers and dequantizes them into shared
-// memory (exact in bf16), computes S^T = C Q^T with one tcgen05 MMA chain
-// (M = 128 entries, N = 64 heads, K = 512, bf16, fp32 accumulate in TMEM),
-// stages S through shared memory for the split's softmax statistics (m, l),
-// and computes O^T = C^T P^T (M = 4 x 128 dims, N = 64 heads, K = 128
-// entries) with P split into bf16 hi + lo parts (the partial output carries
-// ~2^-17 relative error).  One shared-memory copy of C serves both products:
-// K-major for the first, MN-major for the second.  The splits of a query
-// form one thread-block cluster when all clusters of the launch can be
-// resident together: each CTA parks its fp32 partial in its own shared
-// memory and reduces one slice of the dims over its peers through
-// distributed shared memory.  Otherwise the partials go to the workspace and
-// a merge kernel combines them.  Either way the result is rounded once, to
-// fp32 or bf16.
+// query) takes 128 entries: it gathers them and decodes them into shared
+// memory as f16 with the hardware E2M1/E4M3 conversions (every FP4 value
+// times its E4M3 scale and every E4M3 value is exact in f16), converts Q to
+// f16 with a per-query power-of-two scale (exact except for elements far
+// below max|Q|), computes S^T = C Q^T with one tcgen05 MMA chain (M = 128
+// entries, N = 64 heads, K = 512, fp32 accumulate in TMEM), stages S through
+// shared memory for the split's softmax statistics (m, l), and computes
+// O^T = C^T P^T (M = 4 x 128 dims, N = 64 heads, K = 128 entries) with P
+// split into f16 hi + lo parts (the partial output carries ~2^-21 relative
+// error from P).  One shared-memory copy of C serves both products: K-major
+// for the first, MN-major for the second.  The splits of a query form one
+// thread-block cluster when all clusters of the launch can be resident
+// together: each CTA parks its fp32 partial in its own shared memory and
+// reduces one slice of the dims over its peers through distributed shared
+// memory.  Otherwise the partials go to the workspace and a merge kernel
+// combines them.  Either way the result is rounded once, to fp32 or bf16.
 //
 // Optionally the kernel also appends the current token's window latent: the
 // bf16 row for position n-1 is rounded to E4M3 (as csa2_quantize_append FP8
@@ -45,10 +47,10 @@ constexpr int kTcE = 128;          // entries per CTA = M of S^T
 constexpr uint32_t kTcCols = 512;  // TMEM columns: S^T (64) + O^T (4 x 64)
 
 struct AttnTcSmem {
-    uint8_t r0[64 * 1024];         // Q bf16 (B of S^T); then S fp32 [64][128] + P hi/lo f16
-    uint8_t c[kTcE * 1024];        // C [128 entries][512] bf16, then f16
-    uint32_t lut4[256 * 32];       // E2M1 pair -> bf16x2 (unscaled); byte b, lane l at [b * 32 + l]
+    uint8_t r0[64 * 1024];         // Q f16 (B of S^T); then S fp32 [64][128] + P hi/lo f16
+    uint8_t c[kTcE * 1024];        // C [128 entries][512] f16; then the fp32 partial (cluster merge)
     int ok[kTcE];                  // entry valid
+    uint32_t qmax[kAttnThreads / 32];  // per-warp max |Q| (bf16 magnitude bits)
     float ml[kH][2];               // this split's (m, l) per head
     uint64_t bar;                  // MMA completion (phase 0: S, phase 1: O)
     uint32_t tmem;
@@ -67,52 +69,51 @@ __device__ __forceinline__ int soff(int h, int e) { return h * kTcE + (e ^ ((h &
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
-}
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
-    return *reinterpret_cast<uint32_t*>(&r);
-}
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
     __nv_bfloat16 h = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// Two E4M3 bytes, one in the low byte of each 16-bit half of x, as bf16x2
-// (exact).  The sign goes to bit 15 and the 7 exponent/mantissa bits to bits
-// 4..10, which is the bf16 pattern of the value times 2^-120 (E4M3 and bf16
-// subnormals line up); one multiply by 2^120 restores it.  The NaN codes
-// (0x7F, 0xFF), which the FP8 append never writes, read as +-480.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t x) {
-    const uint32_t sgn = x & 0x00800080u;
-    return bf16x2_mul((x + sgn * 15u) << 4, 0x7B807B80u);
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// The eight E2M1 codes of w (low nibble of each byte first) as four f16x2,
+// exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t* o) {
+    asm("{\n .reg .b8 a, b, c, d;\n mov.b32 {a, b, c, d}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, a;\n cvt.rn.f16x2.e2m1x2 %1, b;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, c;\n cvt.rn.f16x2.e2m1x2 %3, d;\n}\n"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
+// The four E4M3 bytes of w (byte 0 first) as two f16x2, exact (E4M3
+// subnormals are f16 normals).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t* o) {
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+        " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}\n"
+        : "=r"(o[0]), "=r"(o[1]) : "r"(w));
 }
 
 // One quarter (128 channels) of an FP4 latent row: 4 x 16 bytes of E2M1
-// codes and 8 E4M3 scales, as bf16 into row e of C.  `lut` is the calling
-// lane's column of the pair table, so the 32 lanes of a warp read 32
-// distinct banks whatever the codes.
-__device__ __forceinline__ void fp4_quarter_to_c(const uint4 (&v)[4], uint2 sc, const uint32_t* lut, uint8_t* c,
-                                                 int e, int qq) {
-    const uint32_t scw[2] = {sc.x, sc.y};
+// codes and 8 E4M3 scales, as f16 into row e of C.  Code times scale has at
+// most 5 significant bits and lies in [2^-10, 2688]: exact in f16.
+__device__ __forceinline__ void fp4_quarter_to_c(const uint4* v, uint2 sc, uint8_t* c, int e, int qq) {
+    uint32_t sw[4];  // scales of groups (0,1), (2,3), (4,5), (6,7) as f16x2
+    e4m3x4_to_f16x2(sc.x, sw);
+    e4m3x4_to_f16x2(sc.y, sw + 2);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {  // scale groups 2j, 2j+1 of this quarter
-            const uint32_t sb = (scw[(2 * j + h) >> 2] >> (8 * ((2 * j + h) & 3))) & 0xFF;
-            const uint32_t s16 = bf16_bits(e4m3_value(sb));
-            const uint32_t s2 = s16 | (s16 << 16);
+            const uint32_t s2 = __byte_perm(sw[j], 0, h ? 0x3232 : 0x1010);
             uint32_t outw[8];
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
-                const uint32_t w = wv[2 * h + m];
+                e2m1x8_to_f16x2(wv[2 * h + m], outw + 4 * m);
 #pragma unroll
-                for (int bb = 0; bb < 4; ++bb) outw[4 * m + bb] = bf16x2_mul(lut[((w >> (8 * bb)) & 0xFF) * 32], s2);
+                for (int bb = 0; bb < 4; ++bb) outw[4 * m + bb] = h2_mul(outw[4 * m + bb], s2);
             }
             const int chunk = qq * 16 + 4 * j + 2 * h;
             *reinterpret_cast<uint4*>(c + row512(e, chunk)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
@@ -121,18 +122,15 @@ __device__ __forceinline__ void fp4_quarter_to_c(const uint4 (&v)[4], uint2 sc, 
     }
 }
 
-// One quarter (128 channels) of an FP8 window row (8 x 16 bytes) as bf16
+// One quarter (128 channels) of an FP8 window row (8 x 16 bytes) as f16
 // into row e of C.
-__device__ __forceinline__ void fp8_quarter_to_c(const uint4 (&v)[8], uint8_t* c, int e, int qq) {
+__device__ __forceinline__ void fp8_quarter_to_c(const uint4* v, uint8_t* c, int e, int qq) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
         uint32_t outw[8];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            outw[2 * m] = e4m3x2_to_bf16x2(__byte_perm(wv[m], 0, 0x4140));
-            outw[2 * m + 1] = e4m3x2_to_bf16x2(__byte_perm(wv[m], 0, 0x4342));
-        }
+        for (int m = 0; m < 4; ++m) e4m3x4_to_f16x2(wv[m], outw + 2 * m);
         const int chunk = qq * 16 + 2 * j;
         *reinterpret_cast<uint4*>(c + row512(e, chunk)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         *reinterpret_cast<uint4*>(c + row512(e, chunk + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
@@ -160,33 +158,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         mbar_init(&S.bar, 1);
         mbar_init_fence();
     }
-    {  // E2M1 pair -> bf16x2 (exact), one copy per lane
-        auto e2m1 = [](int c) {  // magnitude bits: 2 exponent (bias 1), 1 mantissa
-            const int ex = (c >> 1) & 3, m = c & 1;
-            const float v = ex == 0 ? 0.5f * float(m) : ldexpf(1.f + 0.5f * float(m), ex - 1);
-            return (c & 8) ? -v : v;
-        };
-        for (int i = tid; i < 256 * 32; i += kAttnThreads) {
-            const int b = i >> 5;
-            S.lut4[i] = uint32_t(bf16_bits(e2m1(b & 15))) | (uint32_t(bf16_bits(e2m1(b >> 4))) << 16);
-        }
-    }
     grid_dep_wait();
     grid_dep_launch();
-    // the query's row range and this thread's two top-k entries, first
+    // every load of the thread first: the query's row range, its entry, Q
     const int64_t ks = kv_start[q];
     const int32_t nv = n_visible[q];
     // the sequence (top-k entries, then window entries) in groups of 32:
     // split s takes groups s, s + splits, s + 2 splits, s + 3 splits, so the
     // splits get about the same mix and each warp one kind of entry
-    const int pre_ge = (((tid & (kTcE - 1)) >> 5) * splits + split) * 32 + (tid & 31);  // this thread's entry
-    const int32_t pre = pre_ge < k ? topk[q * k + pre_ge] : -1;
+    const int ent = tid & (kTcE - 1), qa = tid >> 7;  // entry; channel quarters qa, qa + 2
+    const int ge = ((ent >> 5) * splits + split) * 32 + (ent & 31);
+    const int32_t pre = ge < k ? topk[q * k + ge] : -1;
     if (warp == 0) tmem_alloc(&S.tmem, kTcCols);
-    // Q (bf16 [64][512]) into the canonical K-major layout, asynchronously
-    const uint16_t* qsrc = qg + q * (kH * kD);
-    for (int i = tid; i < kH * kD / 8; i += kAttnThreads) {
-        const int h = i >> 6, c = i & 63;
-        cp_async16(smem_addr(S.r0 + row512(h, c)), qsrc + h * kD + c * 8);
+    uint4 qv[16];  // Q chunks tid + 256 j: head (tid + 256 j) / 64, channels 8 ((tid + 256 j) % 64) ..
+    {
+        const uint4* qsrc = reinterpret_cast<const uint4*>(qg + q * (kH * kD));
+#pragma unroll
+        for (int j = 0; j < 16; ++j) qv[j] = __ldg(qsrc + tid + j * kAttnThreads);
     }
     int32_t n = 0;  // per-query validity, reported once per query
     {
@@ -207,72 +195,101 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         const int cur_ge = k + nw - 1, grp = cur_ge >> 5;
         if (grp % splits == split) cur_e = (grp / splits) * 32 + (cur_ge & 31);
     }
-    if (cur_e >= 0) {  // E4M3 of its bf16 latent, two channels per thread: to the ring and into C
+    // this thread's row: 0 none (zeros), 1 FP4 latent, 2 FP8 window, 3 the current token
+    int kind = 0;
+    uint4 rv[16];
+    uint2 rs0 = make_uint2(0, 0), rs1 = make_uint2(0, 0);
+    if (ge < k) {
+        const int32_t p = pre;
+        if (p >= 0 && p < n) {
+            kind = 1;
+            const int64_t row = ks + p;
+            const uint4* src = reinterpret_cast<const uint4*>(kv_codes + row * 256);
+            const uint2* ssrc = reinterpret_cast<const uint2*>(kv_scales + row * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                rv[j] = __ldg(src + qa * 4 + j);
+                rv[4 + j] = __ldg(src + (qa + 2) * 4 + j);
+            }
+            rs0 = __ldg(ssrc + qa);
+            rs1 = __ldg(ssrc + qa + 2);
+        } else if (p < -1 || p >= n) {
+            if (qa == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_TOPK, int32_t(q), p);
+        }
+    } else if (ge - k < nw) {
+        if (ent == cur_e) {
+            kind = 3;
+        } else {
+            kind = 2;
+            const int64_t pos = int64_t(n - nw) + (ge - k);
+            const uint4* ring = reinterpret_cast<const uint4*>(swa + (q * window + pos % window) * kD);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                rv[j] = ring[qa * 8 + j];
+                rv[8 + j] = ring[(qa + 2) * 8 + j];
+            }
+        }
+    }
+    if (cur_e >= 0) {  // E4M3 of the current token's bf16 latent, two channels per thread: to the ring and into C
         uint8_t* ring = swa + (q * window + int64_t(n - 1) % window) * kD;
         const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid);
         const uint32_t b2 = e4m3x2_rn_sat(bf16_lo(x), bf16_hi(x));
         reinterpret_cast<uint16_t*>(ring)[tid] = static_cast<uint16_t>(b2);
-        *reinterpret_cast<uint32_t*>(S.c + row512(cur_e, tid >> 2) + (tid & 3) * 4) =
-            e4m3x2_to_bf16x2((b2 & 0xFFu) | ((b2 & 0xFF00u) << 8));
+        uint32_t h2[2];
+        e4m3x4_to_f16x2(b2, h2);
+        *reinterpret_cast<uint32_t*>(S.c + row512(cur_e, tid >> 2) + (tid & 3) * 4) = h2[0];
     }
-    __syncthreads();  // pair table ready
-    // gather + dequantize: thread -> entry e = tid % 128 and channel quarters
-    // qa, qa + 2 (qa = tid / 128); consecutive lanes take consecutive entries,
-    // so each 16-byte store of a warp phase lands on distinct banks.  All
-    // loads of a thread are issued before its first conversion.
+    // Q is stored as f16 times 2^-qs, qs chosen so that max|Q| 2^-qs lies in
+    // [2^14, 2^15): exact for every element above max|Q| 2^-28, the rest within
+    // 2^-25 absolute (scaled), far below the fp32 accumulation error
     {
-        const int e = tid & (kTcE - 1), qa = tid >> 7;
-        const int ge = pre_ge;
-        const uint32_t* lut = S.lut4 + lane;
-        bool ok = false;
-        if (ge < k) {
-            const int32_t p = pre;
-            if (p >= 0 && p < n) {
-                ok = true;
-                const int64_t row = ks + p;
-                const uint4* src = reinterpret_cast<const uint4*>(kv_codes + row * 256);
-                const uint2* ssrc = reinterpret_cast<const uint2*>(kv_scales + row * 32);
-                uint4 v0[4], v1[4];
+        uint32_t am = 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    v0[j] = __ldg(src + qa * 4 + j);
-                    v1[j] = __ldg(src + (qa + 2) * 4 + j);
-                }
-                const uint2 s0 = __ldg(ssrc + qa), s1 = __ldg(ssrc + qa + 2);
-                fp4_quarter_to_c(v0, s0, lut, S.c, e, qa);
-                fp4_quarter_to_c(v1, s1, lut, S.c, e, qa + 2);
-            } else if (p < -1 || p >= n) {
-                if (qa == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_TOPK, int32_t(q), p);
-            }
-        } else if (ge - k < nw) {
-            ok = true;
-            const int64_t pos = int64_t(n - nw) + (ge - k);
-            const int64_t slot = pos % window;
-            const uint8_t* ring = swa + (q * window + slot) * kD;
-            if (e == cur_e) {
-                // the current token: encoded and placed above
-            } else {
-                const uint4* src0 = reinterpret_cast<const uint4*>(ring + qa * 128);
-                const uint4* src1 = reinterpret_cast<const uint4*>(ring + (qa + 2) * 128);
-                uint4 v0[8], v1[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    v0[j] = src0[j];
-                    v1[j] = src1[j];
-                }
-                fp8_quarter_to_c(v0, S.c, e, qa);
-                fp8_quarter_to_c(v1, S.c, e, qa + 2);
-            }
+        for (int j = 0; j < 16; ++j) {
+            am = __vmaxu2(am, __vmaxu2(qv[j].x & 0x7FFF7FFFu, qv[j].y & 0x7FFF7FFFu));
+            am = __vmaxu2(am, __vmaxu2(qv[j].z & 0x7FFF7FFFu, qv[j].w & 0x7FFF7FFFu));
         }
-        if (!ok) {
-#pragma unroll 1
-            for (int h2 = 0; h2 < 2; ++h2)
-                for (int c = (qa + 2 * h2) * 16; c < (qa + 2 * h2) * 16 + 16; ++c)
-                    *reinterpret_cast<uint4*>(S.c + row512(e, c)) = make_uint4(0, 0, 0, 0);
-        }
-        if (qa == 0) S.ok[e] = ok;
+        am = __reduce_max_sync(0xffffffffu, max(am & 0xFFFFu, am >> 16));
+        if (lane == 0) S.qmax[warp] = am;
     }
-    cp_async_wait_all();
+    __syncthreads();  // max |Q| per warp, the current token's row, the barrier
+    int qs = 0;
+    {
+        uint32_t am = 0;
+#pragma unroll
+        for (int w = 0; w < kAttnThreads / 32; ++w) am = max(am, S.qmax[w]);
+        if (am != 0) qs = int(am >> 7) - 127 - 14;  // bf16 exponent of max|Q| minus 14
+        qs = qs < -126 ? -126 : (qs > 126 ? 126 : qs);
+        const float qf = __uint_as_float(uint32_t(127 - qs) << 23);  // 2^-qs
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = tid + j * kAttnThreads;
+            const uint32_t wv[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const __half2 h = __floats2half2_rn(__uint_as_float(wv[m] << 16) * qf,
+                                                    __uint_as_float(wv[m] & 0xFFFF0000u) * qf);
+                o[m] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(S.r0 + row512(i >> 6, i & 63)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    // dequantize this thread's row into C
+    if (kind == 1) {
+        fp4_quarter_to_c(rv, rs0, S.c, ent, qa);
+        fp4_quarter_to_c(rv + 4, rs1, S.c, ent, qa + 2);
+    } else if (kind == 2) {
+        fp8_quarter_to_c(rv, S.c, ent, qa);
+        fp8_quarter_to_c(rv + 8, S.c, ent, qa + 2);
+    } else if (kind == 0) {
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2)
+            for (int c = (qa + 2 * h2) * 16; c < (qa + 2 * h2) * 16 + 16; ++c)
+                *reinterpret_cast<uint4*>(S.c + row512(ent, c)) = make_uint4(0, 0, 0, 0);
+    }
+    if (qa == 0) S.ok[ent] = kind != 0;
+    const float sm_eff = sm_scale * __uint_as_float(uint32_t(127 + qs) << 23);  // logits scale of the f16 S
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -282,7 +299,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 
     // S^T = C Q^T: 32 MMAs of K = 16 dims
     if (tid == 0) {
-        constexpr uint32_t id = idesc_f16(128, 64, 1, false, false);
+        constexpr uint32_t id = idesc_f16(128, 64, 0, false, false);
         for (int kk = 0; kk < kD / 16; ++kk)
             mma_f16_ss(tmem, umma_desc(sm_c + kk * 256, 128, 8192), umma_desc(sm_r0 + kk * 256, 128, 8192), id,
                        kk > 0);
@@ -311,7 +328,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int e = c0 + 4 * j;
-            x[j] = S.ok[e] ? sm_scale * Ssm[soff(h, e)] : -INFINITY;
+            x[j] = S.ok[e] ? sm_eff * Ssm[soff(h, e)] : -INFINITY;
             m = fmaxf(m, x[j]);
         }
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -322,9 +339,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             const int e = c0 + 4 * j;
             const float p = x[j] == -INFINITY ? 0.f : __expf(x[j] - m);
             l += p;
-            const uint16_t hi = bf16_bits(p);
-            *reinterpret_cast<uint16_t*>(p_hi + poff(h, e)) = hi;
-            *reinterpret_cast<uint16_t*>(p_lo + poff(h, e)) = bf16_bits(p - __uint_as_float(uint32_t(hi) << 16));
+            const __half hi = __float2half_rn(p);
+            *reinterpret_cast<__half*>(p_hi + poff(h, e)) = hi;
+            *reinterpret_cast<__half*>(p_lo + poff(h, e)) = __float2half_rn(p - __half2float(hi));
         }
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
@@ -346,7 +363,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 
     // O^T = C^T P^T: 4 blocks of 128 dims; C is the MN-major A operand
     if (tid == 0 && ok_mma) {
-        constexpr uint32_t id = idesc_f16(128, 64, 1, true, false);
+        constexpr uint32_t id = idesc_f16(128, 64, 0, true, false);
         const uint32_t ph = smem_addr(p_hi), pl = smem_addr(p_lo);
         for (int mb = 0; mb < 4; ++mb) {
             const uint32_t d = tmem + 64 + 64 * mb;
