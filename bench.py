@@ -302,6 +302,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
+        torch.cuda.nvtx.range_push("csa2_timed")  # lets an ncu launch list select the timed steps
         with torch.cuda.stream(stream):
             for k in range(K):
                 flush.zero_()
@@ -309,6 +310,7 @@ def run_ours(args):
                 g.replay()
                 ev[k][1].record(stream)
         torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_pop()
         t_wall = time.perf_counter() - t_wall
     if world > 1:
         dist.barrier()
@@ -413,6 +415,44 @@ def run_e2e(g, stream, flush, K, wl):
             "d2h_bytes_per_step": d2h, "steps": K}
 
 
+# ----------------------------------------------------------- ncu launch list
+NCU_NAMES = (("score_tc_kernel<false>", "scan_blockmax"), ("score_tc_kernel<true>", "pool_score"),
+             ("score_tc_kernel<0>", "scan_blockmax"), ("score_tc_kernel<1>", "pool_score"),
+             ("select_blocks_kernel", "select_blocks"), ("select_topk_kernel", "select_topk"),
+             ("attn_tc_kernel", "attn_split"), ("attn_merge_kernel", "attn_merge"),
+             ("quantize_fp4_kernel", "quantize_fp4"), ("quantize_fp8_kernel", "quantize_fp8"))
+
+
+def ncu_summary(csv_path, steps):
+    """Per-kernel launches, device time and share from an ncu
+    `--metrics gpu__time_duration.sum --csv` launch list of the timed steps."""
+    import csv
+    rows = []
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for r in csv.DictReader(lines):
+        if r.get("Metric Name") != "gpu__time_duration.sum":
+            continue
+        name = r["Kernel Name"]
+        key = next((ours for pat, ours in NCU_NAMES if pat in name.replace(" ", "")), None)
+        unit = r.get("Metric Unit", "ns")
+        v = float(r["Metric Value"].replace(",", ""))
+        ns = v * {"ns": 1.0, "nsecond": 1.0, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}.get(unit, 1.0)
+        rows.append((key or "other: " + name.split("(")[0][:60], ns))
+    tot = sum(ns for k, ns in rows if not k.startswith("other"))
+    agg = {}
+    for k, ns in rows:
+        a = agg.setdefault(k, [0, 0.0])
+        a[0] += 1
+        a[1] += ns
+    out = [f"{'kernel':<28}{'launches/step':>14}{'us/step':>10}{'us/launch':>11}{'share':>8}"]
+    for k, (cnt, ns) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        share = f"{ns / tot:8.3f}" if not k.startswith("other") else "       -"
+        out.append(f"{k:<28}{cnt / steps:>14.1f}{ns / 1e3 / steps:>10.1f}{ns / 1e3 / cnt:>11.2f}{share}")
+    out.append(f"{'sum of library kernels':<28}{'':>14}{tot / 1e3 / steps:>10.1f}")
+    return "\n".join(out)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,10 +462,15 @@ def main():
     ap.add_argument("--workload", default="128k", choices=["128k", "1m", "tiny", "manyq", "ragged"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-summary", metavar="CSV",
+                    help="summarize an ncu launch list of the timed steps (--steps gives their number) and exit")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--child-queries", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--child-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.ncu_summary:
+        print(ncu_summary(args.ncu_summary, args.steps))
+        return
     if args.warmup < 3 and not args.cpu_baseline_child and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     if args.cpu_baseline_child:

@@ -170,11 +170,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const int ge = ((ent >> 5) * splits + split) * 32 + (ent & 31);
     const int32_t pre = ge < k ? topk[q * k + ge] : -1;
     if (warp == 0) tmem_alloc(&S.tmem, kTcCols);
-    uint4 qv[16];  // Q chunks tid + 256 j: head (tid + 256 j) / 64, channels 8 ((tid + 256 j) % 64) ..
+    // Q chunk j of this thread (16 bytes): head 8 (g / 16) + lane % 8, chunk
+    // 4 (g % 16) + lane / 8 with g = 16 warp + j.  A quarter-warp covers 8
+    // heads (8 distinct bank groups in the canonical layout); an instruction
+    // reads 64 contiguous bytes of each of 8 rows.
+    auto q_chunk = [&](int j) {
+        const int g = 16 * warp + j;
+        return (8 * (g >> 4) + (lane & 7)) * 64 + 4 * (g & 15) + (lane >> 3);
+    };
+    uint4 qv[16];
     {
         const uint4* qsrc = reinterpret_cast<const uint4*>(qg + q * (kH * kD));
 #pragma unroll
-        for (int j = 0; j < 16; ++j) qv[j] = __ldg(qsrc + tid + j * kAttnThreads);
+        for (int j = 0; j < 16; ++j) qv[j] = __ldg(qsrc + q_chunk(j));
     }
     int32_t n = 0;  // per-query validity, reported once per query
     {
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         const float qf = __uint_as_float(uint32_t(127 - qs) << 23);  // 2^-qs
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const int i = tid + j * kAttnThreads;
+            const int i = q_chunk(j);
             const uint32_t wv[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
             uint32_t o[4];
 #pragma unroll
