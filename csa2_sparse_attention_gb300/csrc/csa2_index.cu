@@ -134,42 +134,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const uint32_t tmem = S.tmem;
 
     if (warp == 0) {  // ------------------------------------------ producer
+        // the scan copies a tile with two bulk copies from lane 0; the gather
+        // spreads a tile's 32 copies (16 blocks x codes, scales) over the lanes
         if (lane == 0) {
             mbar_arrive_expect_tx(&S.qbar, 32 * 64);
             bulk_g2s(S.qcodes, q_codes + (q * 32 / 8) * 512, 32 * 64, &S.qbar);
-            for (int i = 0; i < ntiles; ++i) {
-                const int s = i % kTcStages, r = i / kTcStages;
-                if (r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
-                    record(st, CSA2_ERR_TIMEOUT, 10, int32_t(q), i);
-                    S.abort_flag = 1;
-                    break;
-                }
-                const int64_t t = t0 + i;
-                if (!GATHER) {
+        }
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % kTcStages, r = i / kTcStages;
+            int ok = 1;
+            if (lane == 0 && r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
+                record(st, CSA2_ERR_TIMEOUT, 10, int32_t(q), i);
+                S.abort_flag = 1;
+                ok = 0;
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            const int64_t t = t0 + i;
+            if (!GATHER) {
+                if (lane == 0) {
                     const int64_t nvb64 = nblk_vis - t * 16;
                     const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
                     mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
                     bulk_g2s(S.codes[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
                     bulk_g2s(S.scales[s], k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
-                } else {
-                    uint32_t bytes = 0;
-                    int32_t bl[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int64_t ci = t * 16 + j;
-                        bl[j] = ci < C ? S.cand[ci - t0 * 16] : -1;
-                        if (bl[j] >= 0 && bl[j] < nblk_vis) bytes += 512 + 64;
-                        else if (check_cand && (bl[j] < -1 || bl[j] >= nblk_vis))
-                            record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), bl[j]);
-                    }
-                    mbar_arrive_expect_tx(&S.full[s], bytes);  // 0 bytes: the phase completes at once
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        if (bl[j] >= 0 && bl[j] < nblk_vis) {
-                            bulk_g2s(S.codes[s] + j * 512, k_codes + ((ks >> 3) + bl[j]) * 512, 512, &S.full[s]);
-                            bulk_g2s(S.scales[s] + j * 64, k_scales + (ks + 8 * int64_t(bl[j])) * 8, 64, &S.full[s]);
-                        }
-                    }
+                }
+            } else {
+                const int j = lane & 15;  // block j of the tile: lane j its codes, lane 16 + j its scales
+                const int64_t ci = t * 16 + j;
+                const int32_t bl = ci < C ? S.cand[ci - t0 * 16] : -1;
+                const bool live = bl >= 0 && bl < nblk_vis;
+                if (lane < 16 && !live && check_cand && (bl < -1 || bl >= nblk_vis))
+                    record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), bl);
+                const uint32_t bytes = __reduce_add_sync(0xffffffffu, live ? (lane < 16 ? 512u : 64u) : 0u);
+                if (lane == 0) mbar_arrive_expect_tx(&S.full[s], bytes);  // 0 bytes: the phase completes at once
+                __syncwarp();
+                if (live) {
+                    if (lane < 16)
+                        bulk_g2s(S.codes[s] + j * 512, k_codes + ((ks >> 3) + bl) * 512, 512, &S.full[s]);
+                    else
+                        bulk_g2s(S.scales[s] + j * 64, k_scales + (ks + 8 * int64_t(bl)) * 8, 64, &S.full[s]);
                 }
             }
         }
