@@ -151,3 +151,92 @@ def check_status(g):
         assert st[0] == 0, (name, st)
 
 
+
+
+def run_group_graph(wl):
+    """A group stepped the way the bench times it: one eager step (kernel
+    attributes), then one CUDA-graph replay of the step."""
+    import torch
+    from csa2_sparse_attention_gb300.layer_group import LayerGroup
+    g = LayerGroup(wl)
+    for ws in (g.ws_app, g.ws_full, g.ws_re, g.ws_attn):
+        ws.zero_()
+    g.fill()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        g.step(stream)
+    stream.synchronize()
+    g.capture(stream)
+    g.replay()
+    stream.synchronize()
+    return g
+
+
+def verify_query_at_scale(g, wl, q, cache_sample=2048, seed=7):
+    """One query of a full-size group against the oracle.
+
+    The indexer K cache is compared bit-exact on every row (the Full index
+    scores all of them); the main-latent cache on `cache_sample` random rows,
+    the last row and every row the attention layers read; the Full pool and
+    top-k against the oracle's definitions over the whole context; each
+    Reindex top-k against the oracle on the GPU's pool; each attention layer
+    against the oracle on the GPU's index set."""
+    r = W.request_of(wl, q)
+    n = int(wl.contexts[q])
+    P, K = wl.pool_blocks, wl.topk
+    base = 0 if wl.shared_cache else g.row_base[r]
+    assert base % 8 == 0
+    rows = W.cache_rows(wl, r)
+    # indexer K: every row of the query's view
+    kc, ks = O.quantize_fp4(W.indexer_k_rows(wl, r, 0, n))
+    nb = (n + 7) // 8
+    plane = g.ik_codes[base * 64:(base + nb * 8) * 64].cpu().numpy()
+    assert np.array_equal(block8_to_rows(plane, nb * 8)[:n], O.pack_codes(kc)), f"q{q} indexer K bytes"
+    assert np.array_equal(g.ik_scales[base:base + n].cpu().numpy(), ks), f"q{q} indexer K scales"
+    kdq = O.dequantize_fp4(kc, ks)
+    del kc
+    # indices: Full against the global definitions, Reindex on the GPU's pool
+    topk_of = {}
+    for li, mode in enumerate(wl.layers):
+        if mode not in (W.FULL, W.REINDEX):
+            topk_of[li] = topk_of[W.index_source(wl, li)]
+            continue
+        qc, qs = O.quantize_fp4(W.indexer_q(wl, q, li).astype(np.float64))
+        qdq = O.dequantize_fp4(qc, qs)
+        wv = W.indexer_w(wl, q, li).astype(np.float64)
+        gt = g.topk[li][q].cpu().numpy()
+        if mode == W.FULL:
+            pool_o, top_o, scores, bmax = O.index_full(qdq, wv, kdq, n, P, K)
+            gp = g.pool[q].cpu().numpy()
+            check_selection(gp, pool_o, lambda b: bmax[b], kth_value(bmax, P), f"q{q} pool")
+            check_selection(gt, top_o, lambda p: scores[p], kth_value(scores, K), f"q{q} L{li} top-k")
+            gpu_pool = gp
+        else:
+            re_o, cand, sc = O.index_reindex(qdq, wv, kdq, n, gpu_pool, K)
+            smap = dict(zip(cand.tolist(), sc.tolist()))
+            check_selection(gt, re_o, lambda p: smap[p], kth_value(sc, K), f"q{q} L{li} reindex")
+        topk_of[li] = gt
+    del kdq
+    # main latents: the sampled rows and every row the attention reads
+    rng = np.random.default_rng(seed + q)
+    used = np.concatenate([t[t >= 0] for t in topk_of.values()])
+    need = np.unique(np.concatenate([rng.integers(0, n, cache_sample), used, [n - 1]])).astype(np.int64)
+    lat = W.main_latent_rows(wl, r, 0, rows)[need].astype(np.float64)
+    lc, ls = O.quantize_fp4(O.rope(lat, W.latent_positions(wl, r)[need]))
+    del lat
+    import torch
+    idx = torch.as_tensor(base + need, device=g.kv_codes.device)
+    assert np.array_equal(g.kv_codes[idx].cpu().numpy(), O.pack_codes(lc)), f"q{q} main latent bytes"
+    assert np.array_equal(g.kv_scales[idx].cpu().numpy(), ls), f"q{q} main latent scales"
+    row_of = np.full(n, -1, dtype=np.int64)
+    row_of[need] = np.arange(need.size)
+    for li in range(len(wl.layers)):
+        t = topk_of[li]
+        ids = np.where(t >= 0, row_of[np.maximum(t, 0)], -1)
+        ring = O.append_swa_fp8(W.swa_ring(wl, q, li))
+        assert np.array_equal(g.swa[li][q].cpu().numpy(), ring), f"q{q} L{li} window bytes"
+        sel, win = O.attention_inputs(ids, lc, ls, ring, n, wl.window)
+        o_ref, lse_ref = O.sparse_attention(W.attn_q(wl, q, li), sel, win)
+        check_attention(bf16_to_f64(g.out[li][q]), o_ref, f"q{q} L{li} attention")
+        lse = g.lse[li][q].cpu().numpy()
+        assert np.allclose(lse, lse_ref, rtol=1e-5, atol=1e-5), f"q{q} L{li} lse"
