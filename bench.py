@@ -261,6 +261,72 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------- ours
+def run_append(args):
+    """Bulk KV append: 1,048,576 tokens through the RoPE + FP4 main-latent
+    append (rows layout) and the FP4 indexer-key append (BLOCK8), inputs
+    resident in HBM (1.3 GB, larger than L2), one JSON line in tokens/s."""
+    import torch
+    from csa2_sparse_attention_gb300 import abi
+    from csa2_sparse_attention_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.group_1m()
+    n = 1 << 20
+    lat = torch.from_numpy(W.main_latent_rows(wl, 0, 0, n)).to(torch.bfloat16).to(dev)
+    ik = torch.from_numpy(W.indexer_k_rows(wl, 0, 0, n)).to(torch.bfloat16).to(dev)
+    pos = torch.from_numpy(W.latent_positions(wl, 0)[:n]).to(dev)
+    codes = torch.empty((n, 256), dtype=torch.uint8, device=dev)
+    scales = torch.empty((n, 32), dtype=torch.uint8, device=dev)
+    ik_codes = torch.empty(n * 64, dtype=torch.uint8, device=dev)
+    ik_scales = torch.empty((n, 8), dtype=torch.uint8, device=dev)
+    table = torch.empty(abi.csa2_rope_table_bytes(512, n), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    abi.csa2_rope_table_init(10000.0, 512, n, table, stream)
+
+    def step():
+        abi.csa2_quantize_append(lat, n, 512, abi.FMT_FP4, abi.LAYOUT_ROWS, pos, table, n, None, n,
+                                 codes, scales, ws, ws.numel(), stream)
+        abi.csa2_quantize_append(ik, n, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0, None, n,
+                                 ik_codes, ik_scales, ws, ws.numel(), stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    c0 = abi.csa2_launch_count()
+    with ClockSampler(0) as clk:
+        with torch.cuda.stream(stream):
+            for k in range(K):
+                ev[k][0].record(stream)
+                step()
+                ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+    launches = abi.csa2_launch_count() - c0
+    st = abi.csa2_status_fetch(ws)
+    if st[0] != 0:
+        raise RuntimeError(f"append status {st}")
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    tok_s = n * K / (ms / 1000.0)
+    bpt = (1024 + 256 + 32 + 8) + (256 + 64 + 8)  # main in/out + position, indexer in/out
+    pk, pk_kind = peaks()
+    achieved = bpt * tok_s / 1e9
+    print(json.dumps({"metric": "KV-append tokens/s (RoPE + FP4 main latent, FP4 indexer key)", "value": tok_s,
+                      "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+                      "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                      "dtype": "bf16 in, fp32 RoPE (fp64 near ties), E2M1 + E4M3 out", "data": "synthetic",
+                      "config": {"workload": "bulk-append-1m", "tokens": n,
+                                 "l2": "inputs (1.3 GB) larger than L2, no flush"},
+                      "gpu_launches": launches,
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                   "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk_kind,
+                                   "alg_bytes_per_token": bpt},
+                      "clocks": clk.summary()}), flush=True)
+
+
 class L2Flush:
     """Evicts the 129 MB L2 between timed steps, untimed: writes one 256 MB
     buffer, then reads another, so that the next step finds L2 full of
@@ -475,7 +541,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="128k", choices=["128k", "1m", "tiny", "manyq", "ragged"])
+    ap.add_argument("--workload", default="128k", choices=["128k", "1m", "tiny", "manyq", "ragged", "append"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-summary", metavar="CSV",
@@ -495,6 +561,9 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload == "append":
+        run_append(args)
         return
     run_ours(args)
 
