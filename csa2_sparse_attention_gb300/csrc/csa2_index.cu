@@ -20,6 +20,8 @@
 #include "csa2_pipe.cuh"
 #include "csa2_tc.cuh"
 
+#include <cooperative_groups.h>
+
 namespace csa2 {
 
 // Per-query validity shared by every index/attention kernel.
@@ -293,6 +295,10 @@ struct SelShared {
     int misc[kSelWarps];
     int bins[kSelWarps][32];
     uint32_t cand_key[kCandCap];
+    // cluster selection: this CTA's contribution, read by its peers
+    int cl_hist[2][32];    // bucket counts of a round (double-buffered by round parity)
+    uint32_t cl_minmax[2];
+    int cl_cnt[2];         // keys above / equal to the threshold in this CTA's segment
 };
 
 // Key of element i (float scores/maxima, larger first).
@@ -427,9 +433,10 @@ __device__ void radix_threshold(const KeySrc& key, int n, int count, uint32_t& t
 // (per-warp histograms), and keeps the bucket holding the count-th largest
 // key; `above` counts the keys beyond the live range.  At most 7 rounds of
 // two barriers end with lo == hi == T, take_eq = count - above.
-template <int KPT>
+template <int KPT, bool CL>
 __device__ void kary_threshold(const uint32_t* keys, int n, int count, uint32_t& thr, int& take_eq,
                                SelShared& sm) {
+    namespace cg = cooperative_groups;
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
     uint32_t k[KPT];
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -451,11 +458,25 @@ __device__ void kary_threshold(const uint32_t* keys, int n, int count, uint32_t&
     __syncthreads();
     uint32_t lo = uint32_t(__reduce_min_sync(0xffffffffu, sm.wsum[0][lane])) ^ 0x80000000u;
     uint32_t hi = uint32_t(__reduce_max_sync(0xffffffffu, sm.wsum[1][lane])) ^ 0x80000000u;
+    if constexpr (CL) {  // the range over the whole cluster
+        cg::cluster_group cluster = cg::this_cluster();
+        if (tid == 0) {
+            sm.cl_minmax[0] = lo;
+            sm.cl_minmax[1] = hi;
+        }
+        cluster.sync();
+        const int nb = int(cluster.num_blocks());
+        for (int p = 0; p < nb; ++p) {
+            const uint32_t* mm = cluster.map_shared_rank(sm.cl_minmax, p);
+            lo = min(lo, mm[0]);
+            hi = max(hi, mm[1]);
+        }
+    }
     int above = 0;
     // per-warp 32-bin histograms: sm.bins[warp][bin]
     for (int i = tid; i < kSelWarps * 32; i += blockDim.x) sm.bins[i >> 5][i & 31] = 0;
     __syncthreads();
-    while (lo < hi) {
+    for (int round = 0; lo < hi; ++round) {
         const uint32_t width = hi - lo;
         const int bits = 32 - __clz(width);           // width < 2^bits
         const int shift = bits > 5 ? bits - 5 : 0;    // (width >> shift) < 32
@@ -463,12 +484,24 @@ __device__ void kary_threshold(const uint32_t* keys, int n, int count, uint32_t&
         for (int j = 0; j < KPT; ++j)
             if (k[j] >= lo && k[j] <= hi) atomicAdd(&sm.bins[warp][(k[j] - lo) >> shift], 1);
         __syncthreads();
+        int c = 0;
         if (warp == 0) {
-            int c = 0;
             for (int w = 0; w < kSelWarps; ++w) {
                 c += sm.bins[w][lane];
                 sm.bins[w][lane] = 0;  // ready for the next round
             }
+            if constexpr (CL) sm.cl_hist[round & 1][lane] = c;
+        }
+        if constexpr (CL) {  // bucket counts over the whole cluster; the peers decide identically
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();
+            if (warp == 0) {
+                c = 0;
+                const int nb = int(cluster.num_blocks());
+                for (int p = 0; p < nb; ++p) c += cluster.map_shared_rank(&sm.cl_hist[round & 1][0], p)[lane];
+            }
+        }
+        if (warp == 0) {
             // suffix sums from the top bucket down
             int suf = c;
 #pragma unroll
@@ -497,30 +530,10 @@ __device__ void kary_threshold(const uint32_t* keys, int n, int count, uint32_t&
     take_eq = count - above;
 }
 
-// Select `count` of n keys and write out[j] = map(i) for the selected i in
-// increasing i; pads out[count..pad_to) with -1.
-template <class Map>
-__device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, int32_t* out,
-                               Map map, SelShared& sm) {
-    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
-    if (count > n) count = n;
-    if (count <= 0) {
-        for (int i = tid; i < pad_to; i += blockDim.x) out[i] = -1;
-        return;
-    }
-    uint32_t thr = 0;
-    int take_eq = n;  // count == n: every key (all are >= 0) is taken
-    if (count < n) {
-        if (key.s && n <= 8 * kSelThreads)
-            kary_threshold<8>(key.s, n, count, thr, take_eq, sm);
-        else if (key.s && n <= 16 * kSelThreads)
-            kary_threshold<16>(key.s, n, count, thr, take_eq, sm);
-        else if (key.s && n <= 32 * kSelThreads)
-            kary_threshold<32>(key.s, n, count, thr, take_eq, sm);
-        else
-            radix_threshold(key, n, count, thr, take_eq, sm);
-    }
-    // warp-contiguous segments of whole 32-key chunks
+// Keys above / equal to thr per warp-contiguous segment of whole 32-key
+// chunks (sm.wsum[0] / [1] per warp); returns after a block barrier.
+__device__ void segment_counts(const KeySrc& key, int n, uint32_t thr, SelShared& sm) {
+    const int lane = lane_id(), warp = threadIdx.x >> 5;
     const int seg = ((n + kSelWarps - 1) / kSelWarps + 31) & ~31;
     const int lo = min(n, warp * seg), hi = min(n, lo + seg);
     int gt = 0, eq = 0;
@@ -536,6 +549,16 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
         sm.wsum[1][warp] = eq;
     }
     __syncthreads();
+}
+
+// With segment_counts done: writes out[out_base + j] = map(i) for the keys
+// above thr and the first take_eq keys equal to it, in increasing i.
+template <class Map>
+__device__ void segment_emit(const KeySrc& key, int n, uint32_t thr, int take_eq, int out_base, int32_t* out,
+                             Map map, SelShared& sm) {
+    const int lane = lane_id(), warp = threadIdx.x >> 5;
+    const int seg = ((n + kSelWarps - 1) / kSelWarps + 31) & ~31;
+    const int lo = min(n, warp * seg), hi = min(n, lo + seg);
     if (warp == 0) {
         // exclusive scans over warps: equal keys before, then selections before
         const int e = sm.wsum[1][lane];
@@ -559,7 +582,7 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
         sm.wsum[2][lane] = is - sel;
     }
     __syncthreads();
-    int eq_run = sm.wsum[1][warp], out_run = sm.wsum[2][warp];
+    int eq_run = sm.wsum[1][warp], out_run = out_base + sm.wsum[2][warp];
     const unsigned lt = lanemask_lt();
     constexpr int U = 4;  // chunks whose ballots are in flight together
     for (int b = lo; b < hi; b += 32 * U) {
@@ -590,6 +613,33 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
             out_run += __popc(selm[u]);
         }
     }
+}
+
+// Select `count` of n keys and write out[j] = map(i) for the selected i in
+// increasing i; pads out[count..pad_to) with -1.
+template <class Map>
+__device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, int32_t* out,
+                               Map map, SelShared& sm) {
+    const int tid = threadIdx.x;
+    if (count > n) count = n;
+    if (count <= 0) {
+        for (int i = tid; i < pad_to; i += blockDim.x) out[i] = -1;
+        return;
+    }
+    uint32_t thr = 0;
+    int take_eq = n;  // count == n: every key (all are >= 0) is taken
+    if (count < n) {
+        if (key.s && n <= 8 * kSelThreads)
+            kary_threshold<8, false>(key.s, n, count, thr, take_eq, sm);
+        else if (key.s && n <= 16 * kSelThreads)
+            kary_threshold<16, false>(key.s, n, count, thr, take_eq, sm);
+        else if (key.s && n <= 32 * kSelThreads)
+            kary_threshold<32, false>(key.s, n, count, thr, take_eq, sm);
+        else
+            radix_threshold(key, n, count, thr, take_eq, sm);
+    }
+    segment_counts(key, n, thr, sm);
+    segment_emit(key, n, thr, take_eq, 0, out, map, sm);
     for (int i = count + tid; i < pad_to; i += blockDim.x) out[i] = -1;
 }
 
@@ -630,6 +680,84 @@ __global__ void __launch_bounds__(kSelThreads) select_blocks_kernel(
         __syncthreads();
     }
     select_compact(key, nb, count, count, out + q * out_stride, IdentityMap{}, sm);
+}
+
+struct OffsetMap {
+    int32_t base;
+    __device__ __forceinline__ int32_t operator()(int i) const { return base + i; }
+};
+
+// Top-`count` blocks by block maximum for queries with more blocks than one
+// CTA stages.  The query's blocks are split over a cluster of G CTAs (rank r
+// holds blocks [r S, r S + S), S = seg_keys = 1024 KPT, in shared memory);
+// every threshold round sums its bucket counts over the cluster through
+// distributed shared memory, and each segment's selections are offset by
+// those of the lower ranks, so the output stays ascending.  grid (G, n_q),
+// clusters of G along x, 1024 threads.
+template <int KPT>
+__global__ void __launch_bounds__(kSelThreads) select_blocks_cluster_kernel(
+    const float* __restrict__ blockmax, int64_t nb_stride, const int64_t* __restrict__ kv_start,
+    const int32_t* __restrict__ n_visible, int32_t max_visible, int64_t n_rows, int count,
+    int32_t* __restrict__ out, int64_t out_stride, int seg_keys) {
+    namespace cg = cooperative_groups;
+    extern __shared__ uint32_t smem_keys[];
+    __shared__ SelShared sm;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    const int64_t q = blockIdx.y;
+    const int rank = int(cluster.block_rank());
+    grid_dep_wait();
+    grid_dep_launch();
+    const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
+    const int nb = (n + 7) >> 3;
+    const int s0 = min(nb, rank * seg_keys), s1 = min(nb, s0 + seg_keys), nl = s1 - s0;
+    {  // this segment's keys; s0 is a multiple of 32 and rows start 16-byte aligned
+        const float* v = blockmax + q * nb_stride + s0;
+        const float4* v4 = reinterpret_cast<const float4*>(v);
+        for (int i = tid; i < nl / 4; i += blockDim.x) {
+            const float4 x = v4[i];
+            smem_keys[4 * i] = float_key(x.x);
+            smem_keys[4 * i + 1] = float_key(x.y);
+            smem_keys[4 * i + 2] = float_key(x.z);
+            smem_keys[4 * i + 3] = float_key(x.w);
+        }
+        for (int i = (nl & ~3) + tid; i < nl; i += blockDim.x) smem_keys[i] = float_key(v[i]);
+    }
+    __syncthreads();
+    const int cnt = min(count, nb);  // uniform over the cluster (one query)
+    int32_t* o = out + q * out_stride;
+    if (cnt > 0) {
+        uint32_t thr = 0;
+        int take_eq = nb;  // cnt == nb: every key is taken
+        if (cnt < nb) kary_threshold<KPT, true>(smem_keys, nl, cnt, thr, take_eq, sm);
+        const KeySrc key{nullptr, smem_keys};
+        segment_counts(key, nl, thr, sm);
+        if (warp == 0) {
+            const int gt = __reduce_add_sync(0xffffffffu, sm.wsum[0][lane]);
+            const int eq = __reduce_add_sync(0xffffffffu, sm.wsum[1][lane]);
+            if (lane == 0) {
+                sm.cl_cnt[0] = gt;
+                sm.cl_cnt[1] = eq;
+            }
+        }
+        cluster.sync();
+        if (tid == 0) {  // equal keys and selections in the lower ranks' segments
+            int eq_before = 0, out_before = 0;
+            for (int p = 0; p < rank; ++p) {
+                const int* c = cluster.map_shared_rank(sm.cl_cnt, p);
+                const int t = take_eq - eq_before;
+                out_before += c[0] + (t < 0 ? 0 : (t > c[1] ? c[1] : t));
+                eq_before += c[1];
+            }
+            sm.misc[2] = take_eq - eq_before;
+            sm.misc[3] = out_before;
+        }
+        __syncthreads();
+        segment_emit(key, nl, thr, sm.misc[2], sm.misc[3], o, OffsetMap{s0}, sm);
+    }
+    if (rank == 0)
+        for (int i = cnt + tid; i < count; i += blockDim.x) o[i] = -1;
+    cluster.sync();  // the peers have read this CTA's shared memory
 }
 
 // Top-`count` positions among the scored candidates.  grid n_q, 1024
@@ -713,7 +841,11 @@ static csa2_status prepare_select_kernels() {
         cudaFuncSetAttribute(score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(sizeof(TcScanSmem))) != cudaSuccess ||
         cudaFuncSetAttribute(select_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
-        cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(select_blocks_cluster_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             16 * kSelThreads * 4) != cudaSuccess ||
+        cudaFuncSetAttribute(select_blocks_cluster_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             32 * kSelThreads * 4) != cudaSuccess)
         return CSA2_ERR_CUDA;
     done[dev] = true;
     return CSA2_OK;
@@ -724,6 +856,40 @@ static csa2_status prepare_select_kernels() {
 static int64_t tc_ctas_per_query(int64_t n_q, int64_t tiles_max) {
     int64_t cpq = 2 * kSMs / n_q;
     return cpq < 1 ? 1 : (cpq > tiles_max ? tiles_max : cpq);
+}
+
+// Top-`count` blocks of every query: one CTA per query while a query's
+// blocks fit its shared memory, else a cluster of up to 8 CTAs per query
+// splitting them (16K or 32K keys each), else one CTA selecting from global
+// memory.
+constexpr int kSelClusterMax = 8;
+static void launch_select_blocks(const float* blockmax, int64_t nb_stride, int64_t n_q,
+                                 const int64_t* kv_start, const int32_t* n_visible, int32_t max_visible,
+                                 int64_t n_rows, int count, int32_t* out, int64_t out_stride, cudaStream_t s) {
+    const int64_t nb_max = ceil_div<int64_t>(max_visible, 8);
+    timer_begin(K_SELECT_BLOCKS, s);
+    if (nb_max > kSelSmemKeys) {
+        const int64_t g16 = ceil_div<int64_t>(nb_max, 16 * kSelThreads);
+        const int64_t g32 = ceil_div<int64_t>(nb_max, 32 * kSelThreads);
+        if (g16 <= kSelClusterMax) {
+            launch(select_blocks_cluster_kernel<16>, dim3(unsigned(g16), unsigned(n_q)), kSelThreads,
+                   size_t(16 * kSelThreads) * 4, s, unsigned(g16), blockmax, nb_stride, kv_start, n_visible,
+                   max_visible, n_rows, count, out, out_stride, 16 * kSelThreads);
+            timer_end(K_SELECT_BLOCKS, s);
+            return;
+        }
+        if (g32 <= kSelClusterMax) {
+            launch(select_blocks_cluster_kernel<32>, dim3(unsigned(g32), unsigned(n_q)), kSelThreads,
+                   size_t(32 * kSelThreads) * 4, s, unsigned(g32), blockmax, nb_stride, kv_start, n_visible,
+                   max_visible, n_rows, count, out, out_stride, 32 * kSelThreads);
+            timer_end(K_SELECT_BLOCKS, s);
+            return;
+        }
+    }
+    const int cap_b = sel_cap(nb_stride);
+    launch(select_blocks_kernel, unsigned(n_q), kSelThreads, size_t(cap_b) * 4, s, 1, blockmax, nb_stride,
+           kv_start, n_visible, max_visible, n_rows, count, out, out_stride, cap_b);
+    timer_end(K_SELECT_BLOCKS, s);
 }
 
 // Per-position scores of the candidate blocks, then their top-k (the pool
@@ -782,21 +948,15 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
             blockmax, L.nb_stride, int(cpq), false, st);
         timer_end(K_SCAN, s);
     }
-    const int cap_b = sel_cap(L.nb_stride);
-    timer_begin(K_SELECT_BLOCKS, s);
-    launch(select_blocks_kernel, unsigned(n_q), kSelThreads, size_t(cap_b) * 4, s, 1,
-        blockmax, L.nb_stride, kv_start, n_visible, max_visible, n_rows, pool_blocks, out_pool,
-        pool_blocks, cap_b);
-    timer_end(K_SELECT_BLOCKS, s);
+    launch_select_blocks(blockmax, L.nb_stride, n_q, kv_start, n_visible, max_visible, n_rows, pool_blocks,
+                         out_pool, pool_blocks, s);
     const int32_t* cand = out_pool;
     int64_t cand_stride = pool_blocks;
     if (topk > pool_blocks) {
         // the top-k positions lie in the top-max(P, K) blocks
         int32_t* wide = reinterpret_cast<int32_t*>(base + L.cand);
-        timer_begin(K_SELECT_BLOCKS, s);
-        launch(select_blocks_kernel, unsigned(n_q), kSelThreads, size_t(cap_b) * 4, s, 1,
-            blockmax, L.nb_stride, kv_start, n_visible, max_visible, n_rows, topk, wide, topk, cap_b);
-        timer_end(K_SELECT_BLOCKS, s);
+        launch_select_blocks(blockmax, L.nb_stride, n_q, kv_start, n_visible, max_visible, n_rows, topk, wide,
+                             topk, s);
         cand = wide;
         cand_stride = topk;
     }

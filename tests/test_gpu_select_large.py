@@ -1,0 +1,55 @@
+"""csa2_index_full on contexts whose block maxima do not fit one CTA's shared
+memory: the pool selection then splits each query's blocks over a cluster of
+CTAs (16K or 32K keys each).  The indexer keys repeat 16 distinct rows, so
+the oracle's scores come from a 16-entry table and exact ties are everywhere,
+including across the cluster's segments."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import csa2_oracle as O
+from tests.helpers import check_selection, kth_value, rows_to_block8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("contexts", [(300_000, 50_000, 262_143), (1_600_000, 1_000_003)])
+def test_pool_and_topk_with_cluster_selection(contexts):
+    from csa2_sparse_attention_gb300 import abi
+    rng = np.random.default_rng(sum(contexts))
+    n_q, P, K = len(contexts), 2048, 512
+    distinct = torch.randn((16, 128), generator=torch.Generator().manual_seed(21)).to(torch.bfloat16)
+    kc16, ks16 = O.quantize_fp4(distinct.float().numpy().astype(np.float64))
+    k16 = O.dequantize_fp4(kc16, ks16)
+    pk16 = O.pack_codes(kc16)
+    rows_of = [((n + 7) // 8) * 8 for n in contexts]
+    kv_start = np.concatenate([[0], np.cumsum(rows_of)[:-1]]).astype(np.int64)
+    n_rows = int(sum(rows_of))
+    row_id = rng.integers(0, 16, n_rows)
+    k_codes = torch.from_numpy(rows_to_block8(pk16[row_id])).cuda()
+    k_scales = torch.from_numpy(np.ascontiguousarray(ks16[row_id])).cuda()
+    q_real = torch.randn((n_q * 32, 128), generator=torch.Generator().manual_seed(22)).to(torch.bfloat16)
+    qc, qs = O.quantize_fp4(q_real.float().numpy().astype(np.float64))
+    q_codes = torch.from_numpy(rows_to_block8(O.pack_codes(qc))).cuda()
+    q_scales = torch.from_numpy(np.ascontiguousarray(qs)).cuda()
+    w = rng.uniform(0, 1, (n_q, 32)).astype(np.float32)
+    n_vis = np.asarray(contexts, dtype=np.int32)
+    max_visible = int(n_vis.max())
+    ws = torch.zeros(abi.csa2_workspace_bytes(abi.OP_INDEX_FULL, n_q, max_visible, P, K), dtype=torch.uint8,
+                     device="cuda")
+    pool = torch.full((n_q, P), -7, dtype=torch.int32, device="cuda")
+    topk = torch.full((n_q, K), -7, dtype=torch.int32, device="cuda")
+    abi.csa2_index_full(q_codes, q_scales, torch.from_numpy(w).cuda(), n_q, k_codes, k_scales, n_rows,
+                        torch.from_numpy(kv_start).cuda(), torch.from_numpy(n_vis).cuda(), max_visible, P, K,
+                        pool, topk, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert abi.csa2_status_fetch(ws)[0] == 0
+    qdq = O.dequantize_fp4(qc, qs).reshape(n_q, 32, 128)
+    for q, n in enumerate(contexts):
+        table = O.index_scores(qdq[q], w[q].astype(np.float64), k16)  # score of each distinct row
+        scores = table[row_id[kv_start[q]:kv_start[q] + n]]
+        bmax = O.block_max(scores)
+        check_selection(pool[q].cpu().numpy(), O.select_top(bmax, P), lambda b: bmax[b], kth_value(bmax, P),
+                        f"q{q} pool (n={n})")
+        check_selection(topk[q].cpu().numpy(), O.select_top(scores, K), lambda p: scores[p],
+                        kth_value(scores, K), f"q{q} top-k (n={n})")
