@@ -25,11 +25,16 @@
 namespace csa2 {
 
 // Per-query validity shared by every index/attention kernel.
+__device__ __forceinline__ int32_t checked_visible_values(int64_t ks, int32_t n, int64_t q, int32_t max_visible,
+                                                          int64_t n_rows, Status* st, bool report);
 __device__ __forceinline__ int32_t checked_visible(const int64_t* kv_start, const int32_t* n_visible,
                                                    int64_t q, int32_t max_visible, int64_t n_rows,
                                                    Status* st, bool report) {
-    const int64_t ks = kv_start[q];
-    const int32_t n = n_visible[q];
+    return checked_visible_values(kv_start[q], n_visible[q], q, max_visible, n_rows, st, report);
+}
+// The same checks on values already loaded.
+__device__ __forceinline__ int32_t checked_visible_values(int64_t ks, int32_t n, int64_t q, int32_t max_visible,
+                                                          int64_t n_rows, Status* st, bool report) {
     if (ks < 0 || (ks & 7)) {
         if (report) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_KV_START, int32_t(q), int32_t(ks));
         return 0;
@@ -49,7 +54,10 @@ constexpr int kTile = 128;  // positions per tensor-core tile (16 blocks of 8)
 
 // ------------------------------------------------------------ tensor-core scorer
 // Block-scaled FP4 tcgen05 scorer shared by the full scan and the in-pool
-// scoring.  A tile is 16 blocks = 128 positions (M); N = 32 index heads;
+// scoring, on a (CTAs per query, queries) grid of about two CTAs per SM.  For
+// the scan, C carries the query count (0: never rebalance); when the
+// queries' visible counts differ, the CTAs are reassigned so that every CTA
+// gets about the same number of tiles (scan_map).  A tile is 16 blocks = 128 positions (M); N = 32 index heads;
 // K = 128 channels as two kind::mxf4nvf4 MMAs of 64 with one E4M3 scale per
 // 16 channels, so the FP4 codes go from shared memory to the tensor core
 // without dequantization.  Warp 0 streams tiles (contiguous blocks for the
@@ -80,6 +88,95 @@ struct TcScanSmem {
     int abort_flag;
 };
 
+constexpr int kScanMaxQ = kSMs;  // queries the balanced scan mapping handles (one wave of 2 x SMs)
+static_assert(2 * kSMs - kScanMaxQ >= kSMs, "one wave holds the CTAs of every active query");
+
+
+// The balanced scan mapping over a grid of G CTAs (b = this CTA's linear
+// index): query q gets ceil(tiles_q G / T) CTAs (T = all visible tiles; G
+// is replaced by G - active queries when rounding up would need more than G)
+// and each of them a contiguous slice of that query's tiles.  Warp 0 does
+// it with shuffles (lane l holds queries l QPL .. l QPL + QPL - 1) and
+// publishes this CTA's slice.  Returns whether the CTA has tiles.
+__device__ bool scan_map(const int64_t* kv_start, const int32_t* n_visible, int32_t max_visible, int64_t n_rows,
+                         int nq, uint32_t G, uint32_t b, Status* st, int64_t* slice, int64_t& q, int64_t& t0,
+                         int64_t& t1, int32_t& n) {
+    constexpr int QPL = (kScanMaxQ + 31) / 32;
+    // slice (shared memory): q (or -1), t0, t1, n
+    if (threadIdx.x < 32) {
+        const int lane = lane_id();
+        uint32_t tq[QPL];
+        int32_t nv[QPL];
+        uint32_t run = 0;
+#pragma unroll
+        for (int j = 0; j < QPL; ++j) {
+            const int i = lane * QPL + j;
+            nv[j] = i < nq ? checked_visible(kv_start, n_visible, i, max_visible, n_rows, st,
+                                             st != nullptr && blockIdx.x == 0)
+                           : 0;
+            tq[j] = uint32_t((((int64_t(nv[j]) + 7) >> 3) + 15) >> 4);
+            run += tq[j];
+        }
+        auto incl_scan = [&](uint32_t x) {
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            return x;
+        };
+        const uint32_t T = __shfl_sync(0xffffffffu, incl_scan(run), 31);
+        uint32_t c[QPL], csum = 0, cbase = 0;
+        int found = -1;
+        if (T > 0) {
+            auto ctas = [&](uint64_t G) {
+                uint32_t sum = 0;
+#pragma unroll
+                for (int j = 0; j < QPL; ++j) {
+                    const uint64_t v = (uint64_t(tq[j]) * G + T - 1) / T;
+                    c[j] = uint32_t(v < tq[j] ? v : tq[j]);
+                    sum += c[j];
+                }
+                return sum;
+            };
+            csum = ctas(G);
+            uint32_t cin = incl_scan(csum);
+            if (__shfl_sync(0xffffffffu, cin, 31) > G) {
+                uint32_t act = 0;
+#pragma unroll
+                for (int j = 0; j < QPL; ++j) act += tq[j] > 0;
+                act = __reduce_add_sync(0xffffffffu, act);
+                csum = ctas(G > act ? G - act : 1u);
+                cin = incl_scan(csum);
+            }
+            cbase = cin - csum;
+            if (b >= cbase && b < cin) {  // this lane holds the CTA's query
+                uint32_t lo = cbase;
+#pragma unroll
+                for (int j = 0; j < QPL; ++j) {
+                    if (found < 0 && b < lo + c[j]) {
+                        found = j;
+                        const int64_t jj = b - lo;
+                        slice[0] = int64_t(lane) * QPL + j;
+                        slice[1] = jj * tq[j] / c[j];
+                        slice[2] = (jj + 1) * tq[j] / c[j];
+                        slice[3] = nv[j];
+                    }
+                    lo += c[j];
+                }
+            }
+        }
+        if (!__any_sync(0xffffffffu, found >= 0) && lane == 0) slice[0] = -1;
+    }
+    __syncthreads();
+    q = slice[0];
+    t0 = slice[1];
+    t1 = slice[2];
+    n = int32_t(slice[3]);
+    __syncthreads();  // every thread has read the slice before it is written again
+    return q >= 0;
+}
+
 template <bool GATHER>
 __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales,
@@ -90,16 +187,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     bool check_cand, Status* st) {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
-    const int64_t q = blockIdx.y;
     grid_dep_wait();
     grid_dep_launch();
-    const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, GATHER ? nullptr : st,
-                                      !GATHER && blockIdx.x == 0 && threadIdx.x == 0);
+    int64_t q = blockIdx.y, t0, t1;
+    int32_t n;
+    const int64_t ks_row = kv_start[q];  // this grid row's query, loaded alongside the checks below
+    const int32_t n_row = n_visible[q];
+    // the scan of a batch whose contexts differ (C = its query count, at most
+    // kScanMaxQ) spreads all visible tiles over the grid; equal contexts (and
+    // the pool scoring) split each query over its row of the grid
+    bool skewed = false;
+    if (!GATHER && C > 0) {  // every warp checks (no block barrier)
+        const int32_t n0 = n_visible[0];
+        bool diff = false;
+        for (int i = int(lane_id()); i < C; i += 32) diff |= n_visible[i] != n0;
+        skewed = __any_sync(0xffffffffu, diff);
+    }
+    if (skewed) {
+        if (!scan_map(kv_start, n_visible, max_visible, n_rows, int(C), gridDim.x * gridDim.y,
+                      blockIdx.x + gridDim.x * blockIdx.y, st, reinterpret_cast<int64_t*>(S.cand), q, t0, t1, n))
+            return;
+    } else {
+        n = checked_visible_values(ks_row, n_row, q, max_visible, n_rows, GATHER ? nullptr : st,
+                                   !GATHER && blockIdx.x == 0 && threadIdx.x == 0);
+        const int64_t tiles_q = GATHER ? (C + 15) / 16 : ((int64_t(n) + 7) / 8 + 15) / 16;
+        const int64_t per = (tiles_q + ctas_per_query - 1) / ctas_per_query;
+        t0 = int64_t(blockIdx.x) * per;
+        t1 = t0 + per < tiles_q ? t0 + per : tiles_q;
+    }
     const int64_t nblk_vis = (int64_t(n) + 7) >> 3;
-    const int64_t tiles_q = GATHER ? (C + 15) / 16 : (nblk_vis + 15) / 16;
-    const int64_t per = (tiles_q + ctas_per_query - 1) / ctas_per_query;
-    const int64_t t0 = int64_t(blockIdx.x) * per;
-    const int64_t t1 = t0 + per < tiles_q ? t0 + per : tiles_q;
     if (n <= 0 || t0 >= t1) {
         if (GATHER) {  // nothing visible: every score of this range is -inf
             const int64_t end = t1 * 128 < 8 * int64_t(C) ? t1 * 128 : 8 * int64_t(C);
@@ -944,8 +1060,8 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
         timer_begin(K_SCAN, s);
         launch(score_tc_kernel<false>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
-            q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0, 0,
-            blockmax, L.nb_stride, int(cpq), false, st);
+            q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0,
+            n_q <= kScanMaxQ ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st);
         timer_end(K_SCAN, s);
     }
     launch_select_blocks(blockmax, L.nb_stride, n_q, kv_start, n_visible, max_visible, n_rows, pool_blocks,
