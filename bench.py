@@ -306,13 +306,27 @@ def run_append(args):
                 ev[k][1].record(stream)
         torch.cuda.synchronize(dev)
     launches = abi.csa2_launch_count() - c0
+    # each append alone (CUDA events around 10 back-to-back calls)
+    def alone(call):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(10):
+                call()
+            e1.record(stream)
+        stream.synchronize()
+        return 1000 * e0.elapsed_time(e1) / 10
+    main_us = alone(lambda: abi.csa2_quantize_append(lat, n, 512, abi.FMT_FP4, abi.LAYOUT_ROWS, pos, table, n, None, n,
+                                                     codes, scales, ws, ws.numel(), stream))
+    ik_us = alone(lambda: abi.csa2_quantize_append(ik, n, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0, None, n,
+                                                   ik_codes, ik_scales, ws, ws.numel(), stream))
     st = abi.csa2_status_fetch(ws)
     if st[0] != 0:
         raise RuntimeError(f"append status {st}")
     ms = sum(a.elapsed_time(b) for a, b in ev)
     tok_s = n * K / (ms / 1000.0)
-    bpt = (1024 + 256 + 32 + 8) + (256 + 64 + 8)  # main in/out + position, indexer in/out
     pk, pk_kind = peaks()
+    bpt = (1024 + 256 + 32 + 8) + (256 + 64 + 8)  # main in/out + position, indexer in/out
     achieved = bpt * tok_s / 1e9
     print(json.dumps({"metric": "KV-append tokens/s (RoPE + FP4 main latent, FP4 indexer key)", "value": tok_s,
                       "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
@@ -321,6 +335,9 @@ def run_append(args):
                       "config": {"workload": "bulk-append-1m", "tokens": n,
                                  "l2": "inputs (1.3 GB) larger than L2, no flush"},
                       "gpu_launches": launches,
+                      "kernels": {"main_latent_us": main_us, "indexer_key_us": ik_us,
+                                  "main_latent_frac": (1024 + 256 + 32 + 8) * n / (main_us * 1e-6) / 1e9 / pk["hbm_gbs"],
+                                  "indexer_key_frac": (256 + 64 + 8) * n / (ik_us * 1e-6) / 1e9 / pk["hbm_gbs"]},
                       "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                    "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk_kind,
                                    "alg_bytes_per_token": bpt},

@@ -12,6 +12,7 @@
 // (1024 B read + 288 B written per 512-channel row).
 #include "csa2_common.cuh"
 #include "csa2_timer.cuh"
+#include "csa2_layout.cuh"
 
 #include <cmath>
 
@@ -84,7 +85,7 @@ __device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi) {
 
 // FP4 append.  TPR = dim/16 threads per row.
 template <int DIM, bool BLOCK8>
-__global__ void __launch_bounds__(256) quantize_fp4_kernel(
+__global__ void __launch_bounds__(256, 3) quantize_fp4_kernel(
     const uint4* __restrict__ x, int64_t n, const int64_t* __restrict__ pos,
     const float2* __restrict__ table, int n_hi, int64_t max_pos,
     const int64_t* __restrict__ dst_row, int64_t n_rows, uint8_t* __restrict__ codes,
@@ -94,15 +95,30 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(
     grid_dep_wait();
     grid_dep_launch();
     const int g = threadIdx.x % TPR;
-    for (int64_t i = blockIdx.x * int64_t(RPB) + threadIdx.x / TPR; i < n;
-         i += int64_t(gridDim.x) * RPB) {
-        const int64_t row = dst_row ? __ldg(dst_row + i) : i;
+    const int64_t stride = int64_t(gridDim.x) * RPB;
+    // the next row's input, position and destination are loaded while the
+    // current one is converted (two rows in flight per thread)
+    int64_t i = blockIdx.x * int64_t(RPB) + threadIdx.x / TPR;
+    uint4 na = make_uint4(0, 0, 0, 0), nb = na;
+    int64_t np = 0, nrow = 0;
+    auto fetch = [&](int64_t r) {
+        if (r < n) {
+            const uint4* src = x + r * (DIM / 8) + 2 * g;  // 8 bf16 per uint4
+            na = __ldg(src);
+            nb = __ldg(src + 1);
+            np = pos != nullptr ? __ldg(pos + r) : 0;
+            nrow = dst_row ? __ldg(dst_row + r) : r;
+        }
+    };
+    fetch(i);
+    for (; i < n; i += stride) {
+        const uint4 a = na, b = nb;
+        const int64_t p = np, row = nrow;
+        fetch(i + stride);
         if (row < 0 || row >= n_rows) {
             if (g == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_DST_ROW, int32_t(i), int32_t(row));
             continue;
         }
-        const uint4* src = x + i * (DIM / 8) + 2 * g;  // 8 bf16 per uint4
-        const uint4 a = __ldg(src), b = __ldg(src + 1);
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float v[16];
 #pragma unroll
@@ -115,7 +131,6 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(
         if (pos == nullptr) {
             sb = quantize_group16(v, cw);  // bf16 inputs: exact comparisons
         } else {
-            const int64_t p = __ldg(pos + i);
             if (p < 0 || p >= max_pos) {
                 if (g == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POSITION, int32_t(i), int32_t(p));
                 continue;
@@ -126,6 +141,10 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(
             const int64_t rl = (int64_t(n_hi) + (p & 1023)) * (DIM / 2) + 8 * g;
             const float4* th = reinterpret_cast<const float4*>(table + rh);
             const float4* tl = reinterpret_cast<const float4*>(table + rl);
+            // bnd[j] bounds the fp32 error of pair j's two outputs.  The table
+            // entries are within 2^-25 of cos/sin, so c, s carry at most
+            // 1.5 * 2^-23 and y = x0 c - x1 s at most 2.5 * 2^-23 (|x0| + |x1|)
+            // after its two roundings; 2^-21 (|x0| + |x1|) covers that.
             float y[16], bnd[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -137,16 +156,17 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(
                 y[4 * j + 1] = fmaf(x0, s0, x1 * c0);
                 y[4 * j + 2] = fmaf(x2, c1, -x3 * s1);
                 y[4 * j + 3] = fmaf(x2, s1, x3 * c1);
-                bnd[2 * j] = 0x1p-20f * (fabsf(x0) + fabsf(x1));
-                bnd[2 * j + 1] = 0x1p-20f * (fabsf(x2) + fabsf(x3));
+                bnd[2 * j] = 0x1p-21f * (fabsf(x0) + fabsf(x1));
+                bnd[2 * j + 1] = 0x1p-21f * (fabsf(x2) + fabsf(x3));
             }
             float amax = 0.f, bmax = 0.f;
 #pragma unroll
             for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(y[e]));
 #pragma unroll
             for (int j = 0; j < 8; ++j) bmax = fmaxf(bmax, bnd[j]);
-            const float q6 = __fdiv_rn(amax, 6.0f);
-            const float mq = fmaf(q6, 0x1p-21f, bmax * (1.0f / 6.0f) * 1.001f);
+            // amax / 6 by a multiply: its error (< 2^-22 relative) sits inside mq
+            const float q6 = amax * (1.0f / 6.0f);
+            const float mq = fmaf(q6, 0x1p-20f, bmax * (1.0f / 6.0f) * 1.001f);
             sb = e4m3x2_rn_sat(q6, 0.f) & 0xFF;
             // a tie of the scale inside the margin: resolve in fp64
             const uint32_t span = e4m3x2_rn_sat(fmaxf(q6 - mq, 0.f), q6 + mq);
@@ -160,7 +180,8 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(
                     const float r0 = y[2 * j] * inv, r1 = y[2 * j + 1] * inv;
                     cw[j >> 2] |= e2m1x2_rn_sat(r0, r1) << (8 * (j & 3));
                     const float a0 = fabsf(r0), a1 = fabsf(r1);
-                    const float m0 = fmaf(a0, 0x1p-21f, bnd[j] * inv), m1 = fmaf(a1, 0x1p-21f, bnd[j] * inv);
+                    const float m0 = fmaf(a0, 0x1p-22f, bnd[j] * inv * 1.001f);
+                    const float m1 = fmaf(a1, 0x1p-22f, bnd[j] * inv * 1.001f);
                     risky |= e2m1x2_rn_sat(fmaxf(a0 - m0, 0.f), fmaxf(a1 - m1, 0.f)) !=
                              e2m1x2_rn_sat(a0 + m0, a1 + m1);
                 }
@@ -229,11 +250,14 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(
     }
 }
 
-static int grid_for(int64_t rows, int rows_per_block) {
+// Blocks for `rows` rows: one per rows_per_block rows, at most the blocks
+// that are resident at once (per_sm per SM), which then stride the rows.
+static int grid_for(int64_t rows, int rows_per_block, int per_sm = 16) {
     int64_t g = ceil_div<int64_t>(rows, rows_per_block);
-    const int64_t cap = 152 * 16;  // grid-stride beyond 16 resident blocks per SM
+    const int64_t cap = int64_t(kSMs) * per_sm;
     return int(g < 1 ? 1 : (g > cap ? cap : g));
 }
+constexpr int kFp4BlocksPerSm = 3;  // quantize_fp4_kernel's launch bound
 
 }  // namespace csa2
 
@@ -298,13 +322,13 @@ extern "C" csa2_status csa2_quantize_append(const void* x_bf16, int64_t n, int d
     }
     timer_begin(K_QUANT_FP4, s);
     if (dim == 512)
-        launch(quantize_fp4_kernel<512, false>, grid_for(n, 8), 256, 0, s, 1,
+        launch(quantize_fp4_kernel<512, false>, grid_for(n, 8, kFp4BlocksPerSm), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     else if (layout == CSA2_LAYOUT_BLOCK8)
-        launch(quantize_fp4_kernel<128, true>, grid_for(n, 32), 256, 0, s, 1,
+        launch(quantize_fp4_kernel<128, true>, grid_for(n, 32, kFp4BlocksPerSm), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     else
-        launch(quantize_fp4_kernel<128, false>, grid_for(n, 32), 256, 0, s, 1,
+        launch(quantize_fp4_kernel<128, false>, grid_for(n, 32, kFp4BlocksPerSm), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     timer_end(K_QUANT_FP4, s);
     return launch_status();
