@@ -923,6 +923,209 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     select_compact(key, m, min(count, total), count, out + q * out_stride, CandPosMap{cblk}, sm);
 }
 
+// Full scan for many queries over shared caches (prefill chunks): a CTA
+// takes a group of kMqQ = 4 consecutive queries and a range of 128-position
+// K tiles; queries of the group with the same kv_start share each tile in
+// one block-scaled MMA (M = 128 positions, N = 32 x queries <= 128), so the
+// K tile is read once per group instead of once per query.  The accumulator
+// holds one tile (TMEM columns 0..127); the epilogue applies w.ReLU and the
+// 8-position block max per query, masking positions past each query's
+// visible count.  Queries of a group whose kv_start differs are processed
+// as separate runs (the pipeline drains between runs).  grid (chunks,
+// ceil(n_q / 4)), 192 threads, two CTAs per SM.
+constexpr int kMqQ = 4;
+constexpr int kMqMinQueries = 256;  // batches at least this large use this scan
+
+struct MqSmem {
+    uint8_t codes[kTcStages][kTile * 64];
+    uint8_t scales[kTcStages][kTile * 8];
+    uint8_t qcodes[kMqQ * 32 * 64];  // the run's query heads, BLOCK8 = canonical K-major
+    float w[kMqQ * 32];
+    int32_t n[kMqQ];
+    int64_t ks[kMqQ];
+    uint64_t full[kTcStages], empty[kTcStages];
+    uint64_t sfa_ready[kTcSf];
+    uint64_t acc_full, acc_empty, qbar;
+    uint32_t tmem;
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
+    const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales, const float* __restrict__ w,
+    const uint8_t* __restrict__ k_codes, const uint8_t* __restrict__ k_scales, int64_t n_rows,
+    const int64_t* __restrict__ kv_start, const int32_t* __restrict__ n_visible, int32_t max_visible, int64_t n_q,
+    float* __restrict__ out, int64_t out_stride, Status* st) {
+    extern __shared__ __align__(1024) uint8_t mq_smem_raw[];
+    MqSmem& S = *reinterpret_cast<MqSmem*>(mq_smem_raw);
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    const int64_t q0 = int64_t(blockIdx.y) * kMqQ;
+    const int nqg = int(n_q - q0 < kMqQ ? n_q - q0 : kMqQ);
+    grid_dep_wait();
+    grid_dep_launch();
+    if (tid < kMqQ) {
+        const int64_t q = q0 + tid;
+        S.n[tid] = tid < nqg ? checked_visible(kv_start, n_visible, q, max_visible, n_rows, st,
+                                               blockIdx.x == 0) : 0;
+        S.ks[tid] = tid < nqg ? kv_start[q] : -1;
+    }
+    if (tid < kMqQ * 32) S.w[tid] = tid < nqg * 32 ? __ldg(w + q0 * 32 + tid) : 0.f;
+    if (tid == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], 1);
+        }
+        for (int f = 0; f < kTcSf; ++f) mbar_init(&S.sfa_ready[f], 128);
+        mbar_init(&S.acc_full, 1);
+        mbar_init(&S.acc_empty, 128);
+        mbar_init(&S.qbar, 1);
+        S.abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) tmem_alloc(&S.tmem, kTcCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem;
+    const int quad = warp & 3;
+    const uint32_t lane_base = tmem + (uint32_t(32 * quad) << 16);
+    int it = 0;   // tiles issued so far (ring, slot and accumulator phases)
+    int run = 0;  // runs so far (Q phase)
+    for (int r0 = 0; r0 < nqg;) {
+        int r1 = r0 + 1;  // [r0, r1): queries with the same row range start, and something visible
+        while (r1 < nqg && S.ks[r1] == S.ks[r0]) ++r1;
+        int nmax = 0;
+        for (int j = r0; j < r1; ++j) nmax = max(nmax, S.n[j]);
+        const int64_t ks = S.ks[r0];
+        const int64_t nblk = (int64_t(nmax) + 7) >> 3, tiles = (nblk + 15) >> 4;
+        const int64_t per = (tiles + gridDim.x - 1) / gridDim.x;
+        const int64_t t0 = int64_t(blockIdx.x) * per;
+        const int64_t t1 = t0 + per < tiles ? t0 + per : tiles;
+        const int nr = r1 - r0, ntiles = t0 < t1 ? int(t1 - t0) : 0;
+        if (ntiles > 0) {
+            if (run > 0) {
+                tc_fence_before();
+                __syncthreads();  // the previous run has drained (its MMAs and accumulator reads are done)
+                tc_fence_after();
+            }
+            if (S.abort_flag) break;
+            if (warp == 0) {  // ---------------------------------- producer
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&S.qbar, uint32_t(nr) * 32 * 64);
+                    bulk_g2s(S.qcodes, q_codes + ((q0 + r0) * 32 / 8) * 512, uint32_t(nr) * 32 * 64, &S.qbar);
+                    for (int i = 0; i < ntiles; ++i) {
+                        const int g = it + i, s = g % kTcStages, rr = g / kTcStages;
+                        if (rr > 0 && !mbar_wait(&S.empty[s], (rr - 1) & 1)) {
+                            record(st, CSA2_ERR_TIMEOUT, 20, int32_t(q0 + r0), i);
+                            S.abort_flag = 1;
+                            break;
+                        }
+                        const int64_t t = t0 + i;
+                        const int64_t nvb64 = nblk - t * 16;
+                        const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
+                        mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
+                        bulk_g2s(S.codes[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
+                        bulk_g2s(S.scales[s], k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
+                    }
+                }
+            } else if (warp == 1) {  // --------------------------- MMA issue
+                if (lane == 0) {
+                    bool ok = mbar_wait(&S.qbar, run & 1);
+                    const uint32_t id = idesc_mxf4nvf4(128, 32 * nr);
+                    const uint32_t qa = smem_u32(S.qcodes);
+                    for (int i = 0; ok && i < ntiles; ++i) {
+                        const int g = it + i, s = g % kTcStages, f = g % kTcSf;
+                        ok = mbar_wait(&S.full[s], (g / kTcStages) & 1) && mbar_wait(&S.sfa_ready[f], (g / kTcSf) & 1) &&
+                             (g == 0 || mbar_wait(&S.acc_empty, (g - 1) & 1));
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t ka = smem_u32(S.codes[s]);
+                        const uint32_t sfa = tmem + kColSfa + 8 * f, sfb = tmem + kColSfb;
+                        mma_mxf4_ss(tmem + kColAcc, umma_desc(ka, 128, 512), umma_desc(qa, 128, 512), id, sfa, sfb,
+                                    false);
+                        mma_mxf4_ss(tmem + kColAcc, umma_desc(ka + 256, 128, 512), umma_desc(qa + 256, 128, 512), id,
+                                    sfa + 4, sfb + 4, true);
+                        tc_commit(&S.acc_full);
+                        tc_commit(&S.empty[s]);
+                    }
+                    if (!ok) {
+                        record(st, CSA2_ERR_TIMEOUT, 21, int32_t(q0 + r0), 0);
+                        S.abort_flag = 1;
+                    }
+                }
+            } else {  // ------------------------------------------ epilogue
+                const int row = 32 * quad + lane;
+                {  // the run's query scales (B): rows l + 32 i of the run in column i
+                    uint2 qs[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int hr = lane + 32 * i;  // head row within the run
+                        qs[i] = hr < nr * 32
+                                    ? __ldg(reinterpret_cast<const uint2*>(q_scales + ((q0 + r0) * 32 + hr) * 8))
+                                    : make_uint2(0u, 0u);
+                    }
+                    tmem_st4(lane_base + kColSfb, qs[0].x, qs[1].x, qs[2].x, qs[3].x);
+                    tmem_st4(lane_base + kColSfb + 4, qs[0].y, qs[1].y, qs[2].y, qs[3].y);
+                }
+                auto stage_sf = [&](int i) -> bool {
+                    const int g = it + i, s = g % kTcStages, f = g % kTcSf;
+                    if (!mbar_wait(&S.full[s], (g / kTcStages) & 1)) return false;
+                    uint2 r4[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) r4[j] = *reinterpret_cast<const uint2*>(S.scales[s] + (lane + 32 * j) * 8);
+                    tmem_st4(lane_base + kColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
+                    tmem_st4(lane_base + kColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&S.sfa_ready[f]);
+                    return true;
+                };
+                bool ok = true;
+                for (int i = 0; ok && i < kTcSfLead && i < ntiles; ++i) ok = stage_sf(i);
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    if (i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
+                    const int g = it + i;
+                    if (!ok || !mbar_wait(&S.acc_full, g & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int64_t pos = (t0 + i) * kTile + row;
+                    const int64_t b = pos >> 3;
+                    for (int j = 0; j < nr; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_base + kColAcc + 32 * j, r);
+                        tmem_ld_wait();
+                        if (j == nr - 1) {
+                            tc_fence_before();
+                            mbar_arrive(&S.acc_empty);
+                        }
+                        const float* wj = S.w + (r0 + j) * 32;
+                        float x = 0.f;
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) x = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), x);
+                        const int32_t nj = S.n[r0 + j];
+                        float m = pos < nj ? x : -INFINITY;
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                        if ((lane & 7) == 0 && b < ((int64_t(nj) + 7) >> 3)) out[(q0 + r0 + j) * out_stride + b] = m;
+                    }
+                }
+                if (!ok && lane == 0) {
+                    record(st, CSA2_ERR_TIMEOUT, 22, int32_t(q0 + r0), 0);
+                    S.abort_flag = 1;
+                }
+            }
+            it += ntiles;
+            ++run;
+        }
+        r0 = r1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, kTcCols);
+}
+
 // ------------------------------------------------------------ launches
 static csa2_status check_index_args(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
                                     int64_t n_q, const uint8_t* k_codes, const uint8_t* k_scales,
@@ -956,6 +1159,8 @@ static csa2_status prepare_select_kernels() {
                              int(sizeof(TcScanSmem))) != cudaSuccess ||
         cudaFuncSetAttribute(score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(sizeof(TcScanSmem))) != cudaSuccess ||
+        cudaFuncSetAttribute(scan_mq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(MqSmem))) != cudaSuccess ||
         cudaFuncSetAttribute(select_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(select_blocks_cluster_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1055,7 +1260,18 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
     float* blockmax = reinterpret_cast<float*>(base + L.blockmax);
     float* scores = reinterpret_cast<float*>(base + L.scores);
     const int C = pool_blocks > topk ? pool_blocks : topk;
-    if (max_visible > 0) {
+    if (max_visible > 0 && n_q >= kMqMinQueries) {
+        // many queries: groups of 4 share each K tile; about 8 waves of two CTAs per SM
+        const int64_t groups = ceil_div<int64_t>(n_q, kMqQ);
+        const int64_t tiles = ceil_div<int64_t>(max_visible, kTile);
+        int64_t chunks = ceil_div<int64_t>(8 * 2 * kSMs, groups);
+        chunks = chunks < 1 ? 1 : (chunks > tiles ? tiles : chunks);
+        timer_begin(K_SCAN, s);
+        launch(scan_mq_kernel, dim3(unsigned(chunks), unsigned(groups)), kTcThreads, sizeof(MqSmem), s, 1, q_codes,
+               q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, n_q, blockmax, L.nb_stride,
+               st);
+        timer_end(K_SCAN, s);
+    } else if (max_visible > 0) {
         const int64_t cpq = tc_ctas_per_query(n_q, ceil_div<int64_t>(max_visible, kTile));
         const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
         timer_begin(K_SCAN, s);

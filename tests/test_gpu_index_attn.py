@@ -161,3 +161,15 @@ def test_attention_subnormal_window_bytes_and_scales():
             o_ref, _ = O.sparse_attention(qn[b], sel, win)
             assert np.abs(o_ref).max() < 2.0 ** -3 * 6  # built from subnormal-scale values only
             check_attention(bf16_to_f64(out[b]), o_ref, f"subnormal b{b} window {window}")
+
+
+def test_many_queries_each_with_its_own_cache():
+    """256 queries (the many-query scan's batch size) whose caches all
+    differ: every query is its own run inside a group of four."""
+    ctx = [1000 + 7 * i for i in range(256)]
+    wl = W.small_variant(W.group_128k(), ctx, name="many-own-caches", layers=("F", "X", "R"),
+                         pool_blocks=128, topk=512, hot_blocks=2)
+    g = run_group(wl)
+    check_status(g)
+    for q in (0, 1, 130, 255):
+        verify_query(g, wl, q, check_cache=(q == 0))
