@@ -931,9 +931,16 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
 // holds one tile (TMEM columns 0..127); the epilogue applies w.ReLU and the
 // 8-position block max per query, masking positions past each query's
 // visible count.  Queries of a group whose kv_start differs are processed
-// as separate runs (the pipeline drains between runs).  grid (chunks,
-// ceil(n_q / 4)), 192 threads, two CTAs per SM.
+// as separate runs (the pipeline drains between runs).  Warp 0 streams the
+// tiles, warp 1 issues the MMAs, warps 2..17 are the epilogue: warp w reads
+// TMEM lane quadrant w % 4 for query (w - 2) / 4 of the run, holding that
+// query's w in registers; warps 2..5 also stage the tiles' scales.  grid
+// (chunks, ceil(n_q / 4)), 576 threads, one CTA per SM.
 constexpr int kMqQ = 4;
+constexpr int kMqThreads = 64 + kMqQ * 128;
+constexpr int kMqAcc = 2;                         // accumulators (128 TMEM columns each)
+constexpr uint32_t kMqCols = 512;
+constexpr uint32_t kMqColSfa = 256, kMqColSfb = 288;  // scale slots (4 x 8 columns), query scales (8)
 constexpr int kMqMinQueries = 256;  // batches at least this large use this scan
 
 struct MqSmem {
@@ -945,12 +952,12 @@ struct MqSmem {
     int64_t ks[kMqQ];
     uint64_t full[kTcStages], empty[kTcStages];
     uint64_t sfa_ready[kTcSf];
-    uint64_t acc_full, acc_empty, qbar;
+    uint64_t acc_full[kMqAcc], acc_empty[kMqAcc], qbar;
     uint32_t tmem;
     int abort_flag;
 };
 
-__global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
+__global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales, const float* __restrict__ w,
     const uint8_t* __restrict__ k_codes, const uint8_t* __restrict__ k_scales, int64_t n_rows,
     const int64_t* __restrict__ kv_start, const int32_t* __restrict__ n_visible, int32_t max_visible, int64_t n_q,
@@ -975,13 +982,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
             mbar_init(&S.empty[s], 1);
         }
         for (int f = 0; f < kTcSf; ++f) mbar_init(&S.sfa_ready[f], 128);
-        mbar_init(&S.acc_full, 1);
-        mbar_init(&S.acc_empty, 128);
+        for (int a = 0; a < kMqAcc; ++a) {
+            mbar_init(&S.acc_full[a], 1);
+            mbar_init(&S.acc_empty[a], kMqThreads - 64);
+        }
         mbar_init(&S.qbar, 1);
         S.abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == 1) tmem_alloc(&S.tmem, kTcCols);
+    if (warp == 1) tmem_alloc(&S.tmem, kMqCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1034,17 +1043,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
                     const uint32_t qa = smem_u32(S.qcodes);
                     for (int i = 0; ok && i < ntiles; ++i) {
                         const int g = it + i, s = g % kTcStages, f = g % kTcSf;
+                        const int a = g % kMqAcc;
                         ok = mbar_wait(&S.full[s], (g / kTcStages) & 1) && mbar_wait(&S.sfa_ready[f], (g / kTcSf) & 1) &&
-                             (g == 0 || mbar_wait(&S.acc_empty, (g - 1) & 1));
+                             (g < kMqAcc || mbar_wait(&S.acc_empty[a], ((g / kMqAcc) - 1) & 1));
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t ka = smem_u32(S.codes[s]);
-                        const uint32_t sfa = tmem + kColSfa + 8 * f, sfb = tmem + kColSfb;
-                        mma_mxf4_ss(tmem + kColAcc, umma_desc(ka, 128, 512), umma_desc(qa, 128, 512), id, sfa, sfb,
-                                    false);
-                        mma_mxf4_ss(tmem + kColAcc, umma_desc(ka + 256, 128, 512), umma_desc(qa + 256, 128, 512), id,
-                                    sfa + 4, sfb + 4, true);
-                        tc_commit(&S.acc_full);
+                        const uint32_t d = tmem + 128 * a;
+                        const uint32_t sfa = tmem + kMqColSfa + 8 * f, sfb = tmem + kMqColSfb;
+                        mma_mxf4_ss(d, umma_desc(ka, 128, 512), umma_desc(qa, 128, 512), id, sfa, sfb, false);
+                        mma_mxf4_ss(d, umma_desc(ka + 256, 128, 512), umma_desc(qa + 256, 128, 512), id, sfa + 4,
+                                    sfb + 4, true);
+                        tc_commit(&S.acc_full[a]);
                         tc_commit(&S.empty[s]);
                     }
                     if (!ok) {
@@ -1054,7 +1064,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
                 }
             } else {  // ------------------------------------------ epilogue
                 const int row = 32 * quad + lane;
-                {  // the run's query scales (B): rows l + 32 i of the run in column i
+                const int jq = (warp - 2) >> 2;  // this warp's query within the run
+                const bool stager = jq == 0;     // warps 2..5: one per lane quadrant
+                float wh[32];                    // w / 2 of this warp's query (w relu(x) = w/2 (x + |x|))
+#pragma unroll
+                for (int h = 0; h < 32; ++h) wh[h] = jq < nr ? 0.5f * S.w[(r0 + jq) * 32 + h] : 0.f;
+                if (stager) {  // the run's query scales (B): rows l + 32 i of the run in column i
                     uint2 qs[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -1063,8 +1078,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
                                     ? __ldg(reinterpret_cast<const uint2*>(q_scales + ((q0 + r0) * 32 + hr) * 8))
                                     : make_uint2(0u, 0u);
                     }
-                    tmem_st4(lane_base + kColSfb, qs[0].x, qs[1].x, qs[2].x, qs[3].x);
-                    tmem_st4(lane_base + kColSfb + 4, qs[0].y, qs[1].y, qs[2].y, qs[3].y);
+                    tmem_st4(lane_base + kMqColSfb, qs[0].x, qs[1].x, qs[2].x, qs[3].x);
+                    tmem_st4(lane_base + kMqColSfb + 4, qs[0].y, qs[1].y, qs[2].y, qs[3].y);
                 }
                 auto stage_sf = [&](int i) -> bool {
                     const int g = it + i, s = g % kTcStages, f = g % kTcSf;
@@ -1072,43 +1087,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
                     uint2 r4[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) r4[j] = *reinterpret_cast<const uint2*>(S.scales[s] + (lane + 32 * j) * 8);
-                    tmem_st4(lane_base + kColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
-                    tmem_st4(lane_base + kColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
+                    tmem_st4(lane_base + kMqColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
+                    tmem_st4(lane_base + kMqColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&S.sfa_ready[f]);
                     return true;
                 };
                 bool ok = true;
-                for (int i = 0; ok && i < kTcSfLead && i < ntiles; ++i) ok = stage_sf(i);
+                if (stager)
+                    for (int i = 0; ok && i < kTcSfLead && i < ntiles; ++i) ok = stage_sf(i);
+                const int32_t nj = jq < nr ? S.n[r0 + jq] : 0;
+                const int64_t nbj = (int64_t(nj) + 7) >> 3;
+                float* outj = out + (q0 + r0 + jq) * out_stride;
                 for (int i = 0; ok && i < ntiles; ++i) {
-                    if (i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
-                    const int g = it + i;
-                    if (!ok || !mbar_wait(&S.acc_full, g & 1)) {
+                    if (stager && i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
+                    const int g = it + i, a = g % kMqAcc;
+                    if (!ok || !mbar_wait(&S.acc_full[a], (g / kMqAcc) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int64_t pos = (t0 + i) * kTile + row;
-                    const int64_t b = pos >> 3;
-                    for (int j = 0; j < nr; ++j) {
-                        uint32_t r[32];
-                        tmem_ld32(lane_base + kColAcc + 32 * j, r);
+                    uint32_t r[32];
+                    if (jq < nr) {
+                        tmem_ld32(lane_base + 128 * a + 32 * jq, r);
                         tmem_ld_wait();
-                        if (j == nr - 1) {
-                            tc_fence_before();
-                            mbar_arrive(&S.acc_empty);
-                        }
-                        const float* wj = S.w + (r0 + j) * 32;
-                        float x = 0.f;
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&S.acc_empty[a]);  // the accumulator may be overwritten
+                    if (jq < nr) {
+                        float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-                        for (int h = 0; h < 32; ++h) x = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), x);
-                        const int32_t nj = S.n[r0 + j];
+                        for (int h = 0; h < 32; h += 2) {
+                            const float a0 = __uint_as_float(r[h]), a1 = __uint_as_float(r[h + 1]);
+                            x0 = fmaf(wh[h], a0 + fabsf(a0), x0);
+                            x1 = fmaf(wh[h + 1], a1 + fabsf(a1), x1);
+                        }
+                        const float x = x0 + x1;
+                        const int64_t pos = (t0 + i) * kTile + row;
                         float m = pos < nj ? x : -INFINITY;
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                        if ((lane & 7) == 0 && b < ((int64_t(nj) + 7) >> 3)) out[(q0 + r0 + j) * out_stride + b] = m;
+                        const int64_t b = pos >> 3;
+                        if ((lane & 7) == 0 && b < nbj) outj[b] = m;
                     }
                 }
                 if (!ok && lane == 0) {
@@ -1123,7 +1145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) scan_mq_kernel(
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, kTcCols);
+    if (warp == 1) tmem_dealloc(tmem, kMqCols);
 }
 
 // ------------------------------------------------------------ launches
@@ -1261,13 +1283,13 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
     float* scores = reinterpret_cast<float*>(base + L.scores);
     const int C = pool_blocks > topk ? pool_blocks : topk;
     if (max_visible > 0 && n_q >= kMqMinQueries) {
-        // many queries: groups of 4 share each K tile; about 8 waves of two CTAs per SM
+        // many queries: groups of 4 share each K tile; about 8 waves of one CTA per SM
         const int64_t groups = ceil_div<int64_t>(n_q, kMqQ);
         const int64_t tiles = ceil_div<int64_t>(max_visible, kTile);
-        int64_t chunks = ceil_div<int64_t>(8 * 2 * kSMs, groups);
+        int64_t chunks = ceil_div<int64_t>(8 * kSMs, groups);
         chunks = chunks < 1 ? 1 : (chunks > tiles ? tiles : chunks);
         timer_begin(K_SCAN, s);
-        launch(scan_mq_kernel, dim3(unsigned(chunks), unsigned(groups)), kTcThreads, sizeof(MqSmem), s, 1, q_codes,
+        launch(scan_mq_kernel, dim3(unsigned(chunks), unsigned(groups)), kMqThreads, sizeof(MqSmem), s, 1, q_codes,
                q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, n_q, blockmax, L.nb_stride,
                st);
         timer_end(K_SCAN, s);
