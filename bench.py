@@ -487,31 +487,34 @@ def run_ours(args):
 
 
 def run_e2e(g, stream, flush, K, wl):
-    """Same metric through the C-ABI calls with host buffers: every step
-    copies its inputs from pinned host memory and reads its outputs back."""
+    """Same metric through the same calls with host buffers: every step brings
+    its inputs in from pinned host memory and reads all its outputs back.  The
+    copies run on two more streams inside the step's graph (LayerGroup.step_io):
+    each layer's inputs arrive ahead of it and its outputs leave as soon as it
+    is done, while the later layers compute."""
     import torch
-    ins = [g.tok_latent, g.tok_ik] + list(g.tok_swa) + list(g.attn_q) + \
-          [g.iq_bf16[i] for i in g.index_layers] + [g.iw[i] for i in g.index_layers]
-    outs = list(g.out) + list(g.lse)
-    h_in = [t.detach().cpu().pin_memory() for t in ins]
-    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
-    h2d = sum(t.numel() * t.element_size() for t in ins)
-    d2h = sum(t.numel() * t.element_size() for t in outs)
+    host = g.host_buffers()
+    d_app, d_layer, d_out = g.io_tensors()
+    h2d = sum(t.numel() * t.element_size() for t in d_app) + \
+        sum(t.numel() * t.element_size() for tl in d_layer for t in tl)
+    d2h = sum(t.numel() * t.element_size() for tl in d_out for t in tl)
+    copy_streams = (torch.cuda.Stream(stream.device), torch.cuda.Stream(stream.device))
+    g.capture_io(stream, copy_streams, host)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush()
+            g.replay_io()
         for k in range(K):
             flush()
             evs[k][0].record(stream)
-            for d, h in zip(ins, h_in):
-                d.copy_(h, non_blocking=True)
-            g.replay()
-            for d, h in zip(outs, h_out):
-                h.copy_(d, non_blocking=True)
+            g.replay_io()
             evs[k][1].record(stream)
     stream.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in evs)
     return {"value": g.B * K / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K}
+            "d2h_bytes_per_step": d2h, "steps": K,
+            "note": "host copies pipelined with the layers on two copy streams inside the step's graph"}
 
 
 # ----------------------------------------------------------- ncu launch list

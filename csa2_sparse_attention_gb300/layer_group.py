@@ -183,6 +183,81 @@ class LayerGroup:
         for li in range(len(self.layers)):
             self.layer(li, s, swa_append=append and not self.wl.shared_cache)
 
+    def io_tensors(self):
+        """The per-step inputs (append, then per layer) and outputs (per layer)
+        that travel between host and device in step_io()."""
+        ins_app = [self.tok_latent, self.tok_ik] if not self.wl.shared_cache else []
+        ins_layer = []
+        for li in range(len(self.layers)):
+            t = [self.attn_q[li]]
+            if not self.wl.shared_cache:
+                t.append(self.tok_swa[li])
+            if li in self.index_layers:
+                t += [self.iq_bf16[li], self.iw[li]]
+            ins_layer.append(t)
+        outs_layer = [[self.out[li], self.lse[li]] for li in range(len(self.layers))]
+        return ins_app, ins_layer, outs_layer
+
+    def host_buffers(self):
+        """Pinned host copies of io_tensors(), for step_io()."""
+        ins_app, ins_layer, outs_layer = self.io_tensors()
+        pin = lambda ts: [t.detach().cpu().pin_memory() for t in ts]
+        return pin(ins_app), [pin(t) for t in ins_layer], [pin(t) for t in outs_layer]
+
+    def step_io(self, stream, copy_streams, host):
+        """step() with its host I/O pipelined on two more streams: the first
+        brings every layer's inputs in from pinned host memory ahead of the
+        layer, the second returns each layer's outputs as soon as that layer
+        is done, while `stream` computes the later layers.  `host` comes from
+        host_buffers()."""
+        h2d, d2h = copy_streams
+        h_app, h_layer, h_out = host
+        d_app, d_layer, d_out = self.io_tensors()
+        start = torch.cuda.Event()
+        start.record(stream)
+        h2d.wait_event(start)
+        d2h.wait_event(start)
+        ev_in = []
+        with torch.cuda.stream(h2d):
+            for d, h in zip(d_app, h_app):
+                d.copy_(h, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(h2d)
+            ev_in.append(e)
+            for dl, hl in zip(d_layer, h_layer):
+                for d, h in zip(dl, hl):
+                    d.copy_(h, non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(h2d)
+                ev_in.append(e)
+        stream.wait_event(ev_in[0])
+        if not self.wl.shared_cache:
+            self.append_token(stream)
+        for li in range(len(self.layers)):
+            stream.wait_event(ev_in[1 + li])
+            self.layer(li, stream, swa_append=not self.wl.shared_cache)
+            done = torch.cuda.Event()
+            done.record(stream)
+            d2h.wait_event(done)
+            with torch.cuda.stream(d2h):
+                for d, h in zip(d_out[li], h_out[li]):
+                    h.copy_(d, non_blocking=True)
+        for cs in (h2d, d2h):
+            end = torch.cuda.Event()
+            end.record(cs)
+            stream.wait_event(end)
+
+    def capture_io(self, stream, copy_streams, host):
+        """Capture step_io() into a CUDA graph (replayed by replay_io())."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.step_io(stream, copy_streams, host)
+        self.graph_io = g
+        return g
+
+    def replay_io(self):
+        self.graph_io.replay()
+
     def capture(self, stream):
         """Capture step() into a CUDA graph on `stream` (replayed by replay())."""
         g = torch.cuda.CUDAGraph()

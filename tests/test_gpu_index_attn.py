@@ -173,3 +173,24 @@ def test_many_queries_each_with_its_own_cache():
     check_status(g)
     for q in (0, 1, 130, 255):
         verify_query(g, wl, q, check_cache=(q == 0))
+
+
+def test_step_with_pipelined_host_io_matches_plain_step():
+    """LayerGroup.step_io (inputs in and outputs out on two copy streams,
+    captured with the step in one graph) reads back exactly what a plain
+    step computes, for every layer."""
+    wl = W.tiny()
+    g = run_group(wl)
+    plain = [(o.clone(), l.clone()) for o, l in zip(g.out, g.lse)]
+    host = g.host_buffers()
+    for hl in host[2]:  # poison the host outputs
+        for h in hl:
+            h.fill_(float("nan"))
+    stream = torch.cuda.Stream()
+    g.capture_io(stream, (torch.cuda.Stream(), torch.cuda.Stream()), host)
+    g.replay_io()
+    torch.cuda.synchronize()
+    check_status(g)
+    for li, (o, l) in enumerate(plain):
+        assert torch.equal(host[2][li][0], o.cpu()), f"layer {li} output"
+        assert torch.equal(host[2][li][1], l.cpu()), f"layer {li} lse"
