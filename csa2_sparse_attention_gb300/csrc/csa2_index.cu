@@ -410,6 +410,8 @@ struct SelShared {
     int wsum[3][kSelWarps];
     int misc[kSelWarps];
     int bins[kSelWarps][32];
+    int tbins[kSelWarps][33];  // register selection: bucket counts per warp (padded rows)
+    int ttot[2][32];           // register selection: bucket totals of a round (by round parity)
     uint32_t cand_key[kCandCap];
     // cluster selection: this CTA's contribution, read by its peers
     int cl_hist[2][32];    // bucket counts of a round (double-buffered by round parity)
@@ -759,6 +761,169 @@ __device__ void select_compact(const KeySrc& key, int n, int count, int pad_to, 
     for (int i = count + tid; i < pad_to; i += blockDim.x) out[i] = -1;
 }
 
+// ---- selection with the keys in registers (n <= KPT * 1024): thread t
+// holds keys KPT t .. KPT t + KPT - 1, so warp w holds one contiguous
+// segment and the ordered output needs no pass over shared memory.
+
+// Keys of v[KPT t + j] (float_key), 0 past n (below every real key).
+template <int KPT>
+__device__ __forceinline__ void load_keys(const float* __restrict__ v, int n, uint32_t (&k)[KPT]) {
+    static_assert(KPT % 4 == 0, "whole float4s");
+    const int base = KPT * int(threadIdx.x);
+    if (base + KPT <= n) {  // rows start 16-byte aligned and KPT t is a multiple of 4
+        const float4* v4 = reinterpret_cast<const float4*>(v + base);
+#pragma unroll
+        for (int j = 0; j < KPT / 4; ++j) {
+            const float4 x = v4[j];
+            k[4 * j] = float_key(x.x);
+            k[4 * j + 1] = float_key(x.y);
+            k[4 * j + 2] = float_key(x.z);
+            k[4 * j + 3] = float_key(x.w);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) k[j] = base + j < n ? float_key(v[base + j]) : 0u;
+    }
+}
+
+// The threshold of kary_threshold over register-held keys.  Each round the
+// per-warp bucket counts are summed by a transposed read (warp w totals
+// bucket w over all warps), and every warp takes the bucket decision from
+// the 32 totals itself: two block barriers per round.  sm.tbins must be
+// zero on entry; it is zero again on return.
+template <int KPT>
+__device__ void kary_regs(const uint32_t (&k)[KPT], int n, int count, uint32_t& thr, int& take_eq, SelShared& sm) {
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        if (KPT * tid + j < n) {
+            kmin = min(kmin, k[j]);
+            kmax = max(kmax, k[j]);
+        }
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if (lane == 0) {
+        sm.wsum[0][warp] = int(kmin ^ 0x80000000u);
+        sm.wsum[1][warp] = int(kmax ^ 0x80000000u);
+    }
+    __syncthreads();
+    uint32_t lo = uint32_t(__reduce_min_sync(0xffffffffu, sm.wsum[0][lane])) ^ 0x80000000u;
+    uint32_t hi = uint32_t(__reduce_max_sync(0xffffffffu, sm.wsum[1][lane])) ^ 0x80000000u;
+    int above = 0;
+    for (int round = 0; lo < hi; ++round) {
+        const uint32_t width = hi - lo;
+        const int bits = 32 - __clz(width);
+        const int shift = bits > 5 ? bits - 5 : 0;
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)
+            if (k[j] >= lo && k[j] <= hi) atomicAdd(&sm.tbins[warp][(k[j] - lo) >> shift], 1);
+        __syncthreads();
+        int c = sm.tbins[lane][warp];  // bucket `warp` of warp `lane`
+        sm.tbins[lane][warp] = 0;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0) sm.ttot[round & 1][warp] = c;
+        __syncthreads();
+        c = sm.ttot[round & 1][lane];
+        int suf = c;  // keys in buckets lane .. 31
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_down_sync(0xffffffffu, suf, o);
+            if (lane + o < 32) suf += y;
+        }
+        const unsigned ok = __ballot_sync(0xffffffffu, above + suf >= count);
+        const int bsel = 31 - __clz(ok);
+        const int suf_next = __shfl_sync(0xffffffffu, suf, (bsel + 1) & 31);
+        above += bsel < 31 ? suf_next : 0;
+        const uint32_t nlo = lo + (uint32_t(bsel) << shift);
+        const uint32_t nhi = nlo + ((1u << shift) - 1u);
+        lo = nlo;
+        hi = nhi < hi ? nhi : hi;
+    }
+    thr = lo;
+    take_eq = count - above;
+}
+
+// Select `count` of the n register-held keys (larger first, ties to the
+// lower index) and write out[j] = map(i) for the selected i in increasing
+// i; pads out[count..pad_to) with -1.  sm.tbins must be zero on entry.
+template <int KPT, class Map>
+__device__ void select_regs(const uint32_t (&k)[KPT], int n, int count, int pad_to, int32_t* out, Map map,
+                            SelShared& sm) {
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    if (count > n) count = n;
+    if (count <= 0) {
+        for (int i = tid; i < pad_to; i += blockDim.x) out[i] = -1;
+        return;
+    }
+    uint32_t thr = 0;
+    int take_eq = n;  // count == n: every key is taken
+    if (count < n) kary_regs<KPT>(k, n, count, thr, take_eq, sm);
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const bool in = KPT * tid + j < n;
+        gt += in && k[j] > thr;
+        eq += in && k[j] == thr;
+    }
+    int gi = gt, ei = eq;  // inclusive scans over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y1 = __shfl_up_sync(0xffffffffu, gi, o);
+        const int y2 = __shfl_up_sync(0xffffffffu, ei, o);
+        if (lane >= o) {
+            gi += y1;
+            ei += y2;
+        }
+    }
+    if (lane == 31) {
+        sm.wsum[0][warp] = gi;
+        sm.wsum[1][warp] = ei;
+    }
+    __syncthreads();
+    // every warp scans the warp totals: equal keys before each warp, then
+    // selections before each warp
+    const int e = sm.wsum[1][lane];
+    int ie = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, ie, o);
+        if (lane >= o) ie += y;
+    }
+    int tw = take_eq - (ie - e);
+    tw = tw < 0 ? 0 : (tw > e ? e : tw);
+    const int sw = sm.wsum[0][lane] + tw;
+    int is = sw;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, is, o);
+        if (lane >= o) is += y;
+    }
+    const int eq_before = __shfl_sync(0xffffffffu, ie - e, warp) + (ei - eq);
+    int take = take_eq - eq_before;
+    take = take < 0 ? 0 : (take > eq ? eq : take);
+    const int sel = gt + take;
+    int si = sel;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, si, o);
+        if (lane >= o) si += y;
+    }
+    int pos = __shfl_sync(0xffffffffu, is - sw, warp) + si - sel;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const bool in = KPT * tid + j < n;
+        bool s = in && k[j] > thr;
+        if (in && k[j] == thr && take > 0) {
+            s = true;
+            --take;
+        }
+        if (s) out[pos++] = map(KPT * tid + j);
+    }
+    for (int i = count + tid; i < pad_to; i += blockDim.x) out[i] = -1;
+}
+
 struct IdentityMap {
     __device__ __forceinline__ int32_t operator()(int i) const { return i; }
 };
@@ -781,6 +946,20 @@ __global__ void __launch_bounds__(kSelThreads) select_blocks_kernel(
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
     const int nb = (n + 7) >> 3;
     const float* v = blockmax + q * nb_stride;
+    // up to 16 keys per thread: in registers (rows start 16-byte aligned, nb_stride % 4 == 0)
+    for (int i = threadIdx.x; i < kSelWarps * 33; i += blockDim.x) (&sm.tbins[0][0])[i] = 0;
+    if (nb <= 8 * kSelThreads) {
+        uint32_t k[8];
+        load_keys<8>(v, nb, k);
+        select_regs<8>(k, nb, count, count, out + q * out_stride, IdentityMap{}, sm);
+        return;
+    }
+    if (nb <= 16 * kSelThreads) {
+        uint32_t k[16];
+        load_keys<16>(v, nb, k);
+        select_regs<16>(k, nb, count, count, out + q * out_stride, IdentityMap{}, sm);
+        return;
+    }
     KeySrc key{v, nullptr};
     if (nb <= smem_keys_cap) {  // rows start 16-byte aligned (nb_stride % 4 == 0)
         const float4* v4 = reinterpret_cast<const float4*>(v);
@@ -893,6 +1072,15 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
     const int32_t* cq = cand + q * cand_stride;
     const int nb = (n + 7) >> 3;
+    const int m = 8 * C;
+    const float* v = scores + q * score_stride;
+    // the candidates' scores in registers when they fit (16 per thread; m = 8C:
+    // whole float4s, 16-byte aligned rows), loaded before the candidate ids
+    constexpr int KR = 16;
+    uint32_t k[KR];
+    const bool regs = m <= KR * kSelThreads;
+    if (regs) load_keys<KR>(v, m, k);
+    for (int i = threadIdx.x; i < kSelWarps * 33; i += blockDim.x) (&sm.tbins[0][0])[i] = 0;
     int valid = 0;  // positions that exist among the candidates
     for (int i = threadIdx.x; i < C; i += blockDim.x) {
         const int32_t b = cq[i];
@@ -900,13 +1088,15 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
         if (b >= 0 && b < nb) valid += min(8, n - 8 * b);
     }
     for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, o);
-    if (lane_id() == 0) sm.wsum[0][threadIdx.x >> 5] = valid;
+    if (lane_id() == 0) sm.misc[threadIdx.x >> 5] = valid;
     __syncthreads();
     int total = 0;
-    for (int w = 0; w < kSelWarps; ++w) total += sm.wsum[0][w];
+    for (int w = 0; w < kSelWarps; ++w) total += sm.misc[w];
+    if (regs) {
+        select_regs<KR>(k, m, min(count, total), count, out + q * out_stride, CandPosMap{cblk}, sm);
+        return;
+    }
     __syncthreads();
-    const int m = 8 * C;
-    const float* v = scores + q * score_stride;
     KeySrc key{v, nullptr};
     if (m <= smem_keys_cap) {  // m = 8C: whole float4s, 16-byte aligned rows
         const float4* v4 = reinterpret_cast<const float4*>(v);
