@@ -786,39 +786,35 @@ __device__ __forceinline__ void load_keys(const float* __restrict__ v, int n, ui
     }
 }
 
-// The threshold of kary_threshold over register-held keys.  Each round the
-// per-warp bucket counts are summed by a transposed read (warp w totals
-// bucket w over all warps), and every warp takes the bucket decision from
-// the 32 totals itself: two block barriers per round.  sm.tbins must be
-// zero on entry; it is zero again on return.
+// Threshold rounds of kary_threshold over register-held keys, starting
+// from the key range [lo, hi] of the n keys.  Each round the per-warp
+// bucket counts are summed by a transposed read (warp w totals bucket w
+// over all warps) and every warp takes the bucket decision from the 32
+// totals itself: two block barriers per round.  Once the live bucket holds
+// at most kSelList keys they are compacted into shared memory and the later
+// rounds scan only that list.  sm.tbins must be zero on entry; it is zero
+// again on return.
+constexpr int kSelList = kCandCap;  // compacted live keys (sm.cand_key)
 template <int KPT>
-__device__ void kary_regs(const uint32_t (&k)[KPT], int n, int count, uint32_t& thr, int& take_eq, SelShared& sm) {
+__device__ void kary_regs(const uint32_t (&k)[KPT], uint32_t lo, uint32_t hi, int count, uint32_t& thr,
+                          int& take_eq, SelShared& sm) {
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
-    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-        if (KPT * tid + j < n) {
-            kmin = min(kmin, k[j]);
-            kmax = max(kmax, k[j]);
-        }
-    }
-    kmin = __reduce_min_sync(0xffffffffu, kmin);
-    kmax = __reduce_max_sync(0xffffffffu, kmax);
-    if (lane == 0) {
-        sm.wsum[0][warp] = int(kmin ^ 0x80000000u);
-        sm.wsum[1][warp] = int(kmax ^ 0x80000000u);
-    }
-    __syncthreads();
-    uint32_t lo = uint32_t(__reduce_min_sync(0xffffffffu, sm.wsum[0][lane])) ^ 0x80000000u;
-    uint32_t hi = uint32_t(__reduce_max_sync(0xffffffffu, sm.wsum[1][lane])) ^ 0x80000000u;
     int above = 0;
+    int listed = -1;  // keys in sm.cand_key once compacted
     for (int round = 0; lo < hi; ++round) {
         const uint32_t width = hi - lo;
         const int bits = 32 - __clz(width);
         const int shift = bits > 5 ? bits - 5 : 0;
+        if (listed < 0) {
 #pragma unroll
-        for (int j = 0; j < KPT; ++j)
-            if (k[j] >= lo && k[j] <= hi) atomicAdd(&sm.tbins[warp][(k[j] - lo) >> shift], 1);
+            for (int j = 0; j < KPT; ++j)
+                if (k[j] >= lo && k[j] <= hi) atomicAdd(&sm.tbins[warp][(k[j] - lo) >> shift], 1);
+        } else {
+            for (int i = tid; i < listed; i += blockDim.x) {
+                const uint32_t x = sm.cand_key[i];
+                if (x >= lo && x <= hi) atomicAdd(&sm.tbins[warp][(x - lo) >> shift], 1);
+            }
+        }
         __syncthreads();
         int c = sm.tbins[lane][warp];  // bucket `warp` of warp `lane`
         sm.tbins[lane][warp] = 0;
@@ -835,11 +831,38 @@ __device__ void kary_regs(const uint32_t (&k)[KPT], int n, int count, uint32_t& 
         const unsigned ok = __ballot_sync(0xffffffffu, above + suf >= count);
         const int bsel = 31 - __clz(ok);
         const int suf_next = __shfl_sync(0xffffffffu, suf, (bsel + 1) & 31);
+        const int live = __shfl_sync(0xffffffffu, c, bsel);
         above += bsel < 31 ? suf_next : 0;
         const uint32_t nlo = lo + (uint32_t(bsel) << shift);
         const uint32_t nhi = nlo + ((1u << shift) - 1u);
         lo = nlo;
         hi = nhi < hi ? nhi : hi;
+        if (listed < 0 && lo < hi && live <= kSelList) {  // compact the live keys
+            int mine = 0;
+#pragma unroll
+            for (int j = 0; j < KPT; ++j) mine += k[j] >= lo && k[j] <= hi;
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) sm.misc[warp] = incl;
+            __syncthreads();
+            const int wt = sm.misc[lane];
+            int wi = wt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += y;
+            }
+            int pos = __shfl_sync(0xffffffffu, wi - wt, warp) + incl - mine;
+#pragma unroll
+            for (int j = 0; j < KPT; ++j)
+                if (k[j] >= lo && k[j] <= hi) sm.cand_key[pos++] = k[j];
+            listed = live;
+            __syncthreads();
+        }
     }
     thr = lo;
     take_eq = count - above;
@@ -847,19 +870,47 @@ __device__ void kary_regs(const uint32_t (&k)[KPT], int n, int count, uint32_t& 
 
 // Select `count` of the n register-held keys (larger first, ties to the
 // lower index) and write out[j] = map(i) for the selected i in increasing
-// i; pads out[count..pad_to) with -1.  sm.tbins must be zero on entry.
-template <int KPT, class Map>
+// i; pads out[count..pad_to) with -1.  CAP: count is first capped at the
+// number of keys above float_key(-inf) (positions that exist score above
+// -inf).  before_emit() runs before the block barrier that precedes the
+// output (the place to stage what map() reads).  sm.tbins must be zero on
+// entry.
+template <int KPT, bool CAP, class Map, class Pre>
 __device__ void select_regs(const uint32_t (&k)[KPT], int n, int count, int pad_to, int32_t* out, Map map,
-                            SelShared& sm) {
+                            SelShared& sm, Pre before_emit) {
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    const uint32_t neg_inf = float_key(-INFINITY);
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    int nvalid = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        if (KPT * tid + j < n) {
+            kmin = min(kmin, k[j]);
+            kmax = max(kmax, k[j]);
+            nvalid += k[j] > neg_inf;
+        }
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    nvalid = __reduce_add_sync(0xffffffffu, nvalid);
+    if (lane == 0) {
+        sm.wsum[0][warp] = int(kmin ^ 0x80000000u);
+        sm.wsum[1][warp] = int(kmax ^ 0x80000000u);
+        sm.wsum[2][warp] = nvalid;
+    }
+    __syncthreads();
+    const uint32_t lo = uint32_t(__reduce_min_sync(0xffffffffu, sm.wsum[0][lane])) ^ 0x80000000u;
+    const uint32_t hi = uint32_t(__reduce_max_sync(0xffffffffu, sm.wsum[1][lane])) ^ 0x80000000u;
+    if (CAP) count = min(count, __reduce_add_sync(0xffffffffu, sm.wsum[2][lane]));
     if (count > n) count = n;
+    __syncthreads();  // sm.wsum is reused below
     if (count <= 0) {
         for (int i = tid; i < pad_to; i += blockDim.x) out[i] = -1;
         return;
     }
     uint32_t thr = 0;
     int take_eq = n;  // count == n: every key is taken
-    if (count < n) kary_regs<KPT>(k, n, count, thr, take_eq, sm);
+    if (count < n) kary_regs<KPT>(k, lo, hi, count, thr, take_eq, sm);
     int gt = 0, eq = 0;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
@@ -881,6 +932,7 @@ __device__ void select_regs(const uint32_t (&k)[KPT], int n, int count, int pad_
         sm.wsum[0][warp] = gi;
         sm.wsum[1][warp] = ei;
     }
+    before_emit();
     __syncthreads();
     // every warp scans the warp totals: equal keys before each warp, then
     // selections before each warp
@@ -924,6 +976,10 @@ __device__ void select_regs(const uint32_t (&k)[KPT], int n, int count, int pad_
     for (int i = count + tid; i < pad_to; i += blockDim.x) out[i] = -1;
 }
 
+struct NoStage {
+    __device__ __forceinline__ void operator()() const {}
+};
+
 struct IdentityMap {
     __device__ __forceinline__ int32_t operator()(int i) const { return i; }
 };
@@ -951,13 +1007,13 @@ __global__ void __launch_bounds__(kSelThreads) select_blocks_kernel(
     if (nb <= 8 * kSelThreads) {
         uint32_t k[8];
         load_keys<8>(v, nb, k);
-        select_regs<8>(k, nb, count, count, out + q * out_stride, IdentityMap{}, sm);
+        select_regs<8, false>(k, nb, count, count, out + q * out_stride, IdentityMap{}, sm, NoStage{});
         return;
     }
     if (nb <= 16 * kSelThreads) {
         uint32_t k[16];
         load_keys<16>(v, nb, k);
-        select_regs<16>(k, nb, count, count, out + q * out_stride, IdentityMap{}, sm);
+        select_regs<16, false>(k, nb, count, count, out + q * out_stride, IdentityMap{}, sm, NoStage{});
         return;
     }
     KeySrc key{v, nullptr};
@@ -1069,18 +1125,36 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     const int64_t q = blockIdx.x;
     grid_dep_wait();
     grid_dep_launch();
-    const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
-    const int32_t* cq = cand + q * cand_stride;
-    const int nb = (n + 7) >> 3;
     const int m = 8 * C;
     const float* v = scores + q * score_stride;
-    // the candidates' scores in registers when they fit (16 per thread; m = 8C:
-    // whole float4s, 16-byte aligned rows), loaded before the candidate ids
+    const int32_t* cq = cand + q * cand_stride;
     constexpr int KR = 16;
-    uint32_t k[KR];
-    const bool regs = m <= KR * kSelThreads;
-    if (regs) load_keys<KR>(v, m, k);
-    for (int i = threadIdx.x; i < kSelWarps * 33; i += blockDim.x) (&sm.tbins[0][0])[i] = 0;
+    if (m <= KR * kSelThreads) {
+        // the candidates' scores in registers (16 per thread; m = 8C: whole
+        // float4s, 16-byte aligned rows).  Positions that do not exist score
+        // -inf, so the count is capped from the keys themselves, and the
+        // candidate ids (at most 2 per thread) are only staged in shared
+        // memory for the output
+        uint32_t k[KR];
+        load_keys<KR>(v, m, k);
+        int32_t cid[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = int(threadIdx.x) + r * kSelThreads;
+            cid[r] = i < C ? cq[i] : -1;
+        }
+        for (int i = threadIdx.x; i < kSelWarps * 33; i += blockDim.x) (&sm.tbins[0][0])[i] = 0;
+        select_regs<KR, true>(k, m, count, count, out + q * out_stride, CandPosMap{cblk}, sm, [&] {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i = int(threadIdx.x) + r * kSelThreads;
+                if (i < C) cblk[i] = cid[r];
+            }
+        });
+        return;
+    }
+    const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
+    const int nb = (n + 7) >> 3;
     int valid = 0;  // positions that exist among the candidates
     for (int i = threadIdx.x; i < C; i += blockDim.x) {
         const int32_t b = cq[i];
@@ -1092,10 +1166,6 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     __syncthreads();
     int total = 0;
     for (int w = 0; w < kSelWarps; ++w) total += sm.misc[w];
-    if (regs) {
-        select_regs<KR>(k, m, min(count, total), count, out + q * out_stride, CandPosMap{cblk}, sm);
-        return;
-    }
     __syncthreads();
     KeySrc key{v, nullptr};
     if (m <= smem_keys_cap) {  // m = 8C: whole float4s, 16-byte aligned rows
