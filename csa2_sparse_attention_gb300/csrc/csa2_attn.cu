@@ -184,6 +184,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 #pragma unroll
         for (int j = 0; j < 16; ++j) qv[j] = __ldg(qsrc + q_chunk(j));
     }
+    // the current token's bf16 window latent (two channels per thread), loaded
+    // now by the split that holds its entry when the context fills the window
+    // (the usual case), so it does not wait for the context length
+    const bool pre_new = swa_new != nullptr && window > 0 && ((k + window - 1) >> 5) % splits == split;
+    const uint32_t x_new = pre_new ? __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid) : 0u;
     int32_t n = 0;  // per-query validity, reported once per query
     {
         const bool report = split == 0 && tid == 0;
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     }
     if (cur_e >= 0) {  // E4M3 of the current token's bf16 latent, two channels per thread: to the ring and into C
         uint8_t* ring = swa + (q * window + int64_t(n - 1) % window) * kD;
-        const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid);
+        const uint32_t x = pre_new ? x_new : __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid);
         const uint32_t b2 = e4m3x2_rn_sat(bf16_lo(x), bf16_hi(x));
         reinterpret_cast<uint16_t*>(ring)[tid] = static_cast<uint16_t>(b2);
         uint32_t h2[2];
