@@ -13,6 +13,7 @@ that order; all arithmetic runs in libcsa2.so.
 from __future__ import annotations
 
 import math
+from typing import NamedTuple
 
 import numpy as np
 import torch
@@ -23,6 +24,37 @@ from . import workloads as W
 
 def _round8(n):
     return (int(n) + 7) // 8 * 8
+
+
+class _Flat:
+    """Typed tensors carved in order out of one flat byte buffer, each
+    starting 256-byte aligned, so that a run of them moves in one copy."""
+
+    def __init__(self):
+        self.items = []
+        self.size = 0
+
+    def add(self, shape, dtype):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.items.append((self.size, n, tuple(shape), dtype))
+        self.size = (self.size + n + 255) // 256 * 256
+        return len(self.items) - 1
+
+    def offset(self, i):
+        return self.items[i][0] if i < len(self.items) else self.size
+
+    def views(self, buf):
+        return [buf[o:o + n].view(dt).view(sh) for o, n, sh, dt in self.items]
+
+
+class HostIO(NamedTuple):
+    """Pinned host buffers of one step's inputs and outputs: per-tensor views
+    (app inputs, per-layer inputs, per-layer [out, lse]) of two flat buffers."""
+    app: list
+    layers: list
+    outs: list
+    flat_in: torch.Tensor
+    flat_out: torch.Tensor
 
 
 class LayerGroup:
@@ -62,22 +94,40 @@ class LayerGroup:
         abi.csa2_rope_table_init(rope_theta, 512, max_pos, self.rope, torch.cuda.current_stream(d))
         L = len(self.layers)
         self.swa = [torch.zeros((self.B, self.Wn, 512), dtype=u8, device=d) for _ in range(L)]
-        self.attn_q = [torch.zeros((self.B, 64, 512), dtype=torch.bfloat16, device=d) for _ in range(L)]
         self.out_dtype = out_dtype
         self.out_code = abi.OUT_F32 if out_dtype == torch.float32 else abi.OUT_BF16
-        self.out = [torch.zeros((self.B, 64, 512), dtype=out_dtype, device=d) for _ in range(L)]
-        self.lse = [torch.zeros((self.B, 64), dtype=torch.float32, device=d) for _ in range(L)]
         self.index_layers = [i for i, m in enumerate(self.layers) if m in (W.FULL, W.REINDEX)]
-        self.iq_bf16 = {i: torch.zeros((self.B * 32, 128), dtype=torch.bfloat16, device=d) for i in self.index_layers}
+        # the step's inputs and outputs live in two flat buffers, in step
+        # order: [current-token latents] + per layer [attention q, window
+        # latent, (indexer q, w)], and per layer [out, lse]
+        bf = torch.bfloat16
+        fin, fout = _Flat(), _Flat()
+        i_tok = (fin.add((self.B, 512), bf), fin.add((self.B, 128), bf))
+        self._in_layer = []  # (first item index, item indices) per layer
+        for li in range(L):
+            first = len(fin.items)
+            items = [fin.add((self.B, 64, 512), bf), fin.add((self.B, 512), bf)]
+            if li in self.index_layers:
+                items += [fin.add((self.B * 32, 128), bf), fin.add((self.B, 32), torch.float32)]
+            self._in_layer.append((first, items))
+        self._out_layer = [(fout.add((self.B, 64, 512), out_dtype), fout.add((self.B, 64), torch.float32))
+                           for _ in range(L)]
+        self._fin, self._fout = fin, fout
+        self.io_in = torch.zeros(fin.size, dtype=u8, device=d)
+        self.io_out = torch.zeros(fout.size, dtype=u8, device=d)
+        vin, vout = fin.views(self.io_in), fout.views(self.io_out)
+        self.attn_q = [vin[self._in_layer[li][1][0]] for li in range(L)]
+        self.out = [vout[o] for o, _ in self._out_layer]
+        self.lse = [vout[l_] for _, l_ in self._out_layer]
+        self.iq_bf16 = {i: vin[self._in_layer[i][1][2]] for i in self.index_layers}
         self.iq_codes = {i: torch.zeros((self.B * 32 * 64,), dtype=u8, device=d) for i in self.index_layers}
         self.iq_scales = {i: torch.zeros((self.B * 32, 8), dtype=u8, device=d) for i in self.index_layers}
-        self.iw = {i: torch.zeros((self.B, 32), dtype=torch.float32, device=d) for i in self.index_layers}
+        self.iw = {i: vin[self._in_layer[i][1][3]] for i in self.index_layers}
         self.topk = {i: torch.full((self.B, self.K), -1, dtype=torch.int32, device=d) for i in self.index_layers}
         self.pool = torch.full((self.B, self.P), -1, dtype=torch.int32, device=d)
         # current-token inputs of a decode step
-        self.tok_latent = torch.zeros((self.B, 512), dtype=torch.bfloat16, device=d)
-        self.tok_ik = torch.zeros((self.B, 128), dtype=torch.bfloat16, device=d)
-        self.tok_swa = [torch.zeros((self.B, 512), dtype=torch.bfloat16, device=d) for _ in range(L)]
+        self.tok_latent, self.tok_ik = vin[i_tok[0]], vin[i_tok[1]]
+        self.tok_swa = [vin[self._in_layer[li][1][1]] for li in range(L)]
         last = self.contexts - 1
         self.tok_pos = torch.from_numpy(last * wl.m + (wl.m - 1)).to(d)
         self.tok_row = torch.from_numpy(starts + last).to(d)
@@ -199,49 +249,62 @@ class LayerGroup:
         return ins_app, ins_layer, outs_layer
 
     def host_buffers(self):
-        """Pinned host copies of io_tensors(), for step_io()."""
-        ins_app, ins_layer, outs_layer = self.io_tensors()
-        pin = lambda ts: [t.detach().cpu().pin_memory() for t in ts]
-        return pin(ins_app), [pin(t) for t in ins_layer], [pin(t) for t in outs_layer]
+        """Pinned host copies of the step's flat input and output buffers
+        (holding the current inputs), with per-tensor views, for step_io()."""
+        flat_in = self.io_in.cpu().pin_memory()
+        flat_out = self.io_out.cpu().pin_memory()
+        vin, vout = self._fin.views(flat_in), self._fout.views(flat_out)
+        app = vin[:2] if not self.wl.shared_cache else []
+        layers = []
+        for li, (_, items) in enumerate(self._in_layer):
+            t = [vin[items[0]]] + ([vin[items[1]]] if not self.wl.shared_cache else []) + [vin[i] for i in items[2:]]
+            layers.append(t)
+        outs = [[vout[o], vout[l_]] for o, l_ in self._out_layer]
+        return HostIO(app, layers, outs, flat_in, flat_out)
+
+    # layers before which the compute stream waits for the inputs copied so
+    # far: a wait that breaks the chain of programmatic launches costs a few
+    # microseconds, so the inputs come in a few growing groups
+    IO_WAIT_AT = (0, 1, 3, 7, 15)
 
     def step_io(self, stream, copy_streams, host):
         """step() with its host I/O pipelined on two more streams: the first
-        brings every layer's inputs in from pinned host memory ahead of the
-        layer, the second returns each layer's outputs as soon as that layer
-        is done, while `stream` computes the later layers.  `host` comes from
+        brings the inputs in from pinned host memory in a few growing groups
+        of layers (one copy each, ahead of the group), the second returns
+        each layer's [out, lse] in one copy as soon as that layer is done,
+        while `stream` computes the later layers.  `host` comes from
         host_buffers()."""
         h2d, d2h = copy_streams
-        h_app, h_layer, h_out = host
-        d_app, d_layer, d_out = self.io_tensors()
+        L = len(self.layers)
+        waits = [w for w in self.IO_WAIT_AT if w < L]
+        bounds = waits[1:] + [L]
         start = torch.cuda.Event()
         start.record(stream)
         h2d.wait_event(start)
         d2h.wait_event(start)
-        ev_in = []
+        ev_group = {}
         with torch.cuda.stream(h2d):
-            for d, h in zip(d_app, h_app):
-                d.copy_(h, non_blocking=True)
-            e = torch.cuda.Event()
-            e.record(h2d)
-            ev_in.append(e)
-            for dl, hl in zip(d_layer, h_layer):
-                for d, h in zip(dl, hl):
-                    d.copy_(h, non_blocking=True)
+            for k, (w0, w1) in enumerate(zip(waits, bounds)):
+                lo = 0 if k == 0 else self._fin.offset(self._in_layer[w0][0])
+                hi = self._fin.offset(self._in_layer[w1][0]) if w1 < L else self._fin.size
+                self.io_in[lo:hi].copy_(host.flat_in[lo:hi], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(h2d)
-                ev_in.append(e)
-        stream.wait_event(ev_in[0])
+                ev_group[w0] = e
+        stream.wait_event(ev_group[0])
         if not self.wl.shared_cache:
             self.append_token(stream)
-        for li in range(len(self.layers)):
-            stream.wait_event(ev_in[1 + li])
+        for li in range(L):
+            if li in ev_group and li > 0:
+                stream.wait_event(ev_group[li])
             self.layer(li, stream, swa_append=not self.wl.shared_cache)
             done = torch.cuda.Event()
             done.record(stream)
             d2h.wait_event(done)
+            o_, l_ = self._out_layer[li]
+            lo, hi = self._fout.offset(o_), self._fout.offset(l_ + 1)
             with torch.cuda.stream(d2h):
-                for d, h in zip(d_out[li], h_out[li]):
-                    h.copy_(d, non_blocking=True)
+                host.flat_out[lo:hi].copy_(self.io_out[lo:hi], non_blocking=True)
         for cs in (h2d, d2h):
             end = torch.cuda.Event()
             end.record(cs)
