@@ -543,7 +543,7 @@ def run_e2e(g, stream, flush, K, wl):
     return {"value": g.B * K / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
             "note": "host copies pipelined with the layers on two copy streams inside the step's graph: "
-                    "inputs in 5 grouped copies, one output copy per layer"}
+                    "inputs in 5 grouped copies ahead of their use, one output copy per layer"}
 
 
 # ----------------------------------------------------------- ncu launch list

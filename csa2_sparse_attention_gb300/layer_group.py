@@ -97,37 +97,41 @@ class LayerGroup:
         self.out_dtype = out_dtype
         self.out_code = abi.OUT_F32 if out_dtype == torch.float32 else abi.OUT_BF16
         self.index_layers = [i for i, m in enumerate(self.layers) if m in (W.FULL, W.REINDEX)]
-        # the step's inputs and outputs live in two flat buffers, in step
-        # order: [current-token latents] + per layer [attention q, window
-        # latent, (indexer q, w)], and per layer [out, lse]
+        # the step's inputs and outputs live in two flat buffers, in the
+        # order the step uses them: [current-token latents] + per layer
+        # [(indexer q, w), attention q, window latent], and per layer [out, lse]
         bf = torch.bfloat16
         fin, fout = _Flat(), _Flat()
         i_tok = (fin.add((self.B, 512), bf), fin.add((self.B, 128), bf))
-        self._in_layer = []  # (first item index, item indices) per layer
+        self._in_layer = []  # per layer: first item of its index part, of its attention part
+        vid = {}
         for li in range(L):
             first = len(fin.items)
-            items = [fin.add((self.B, 64, 512), bf), fin.add((self.B, 512), bf)]
             if li in self.index_layers:
-                items += [fin.add((self.B * 32, 128), bf), fin.add((self.B, 32), torch.float32)]
-            self._in_layer.append((first, items))
+                vid[li, "iq"] = fin.add((self.B * 32, 128), bf)
+                vid[li, "iw"] = fin.add((self.B, 32), torch.float32)
+            first_attn = len(fin.items)
+            vid[li, "q"] = fin.add((self.B, 64, 512), bf)
+            vid[li, "swa"] = fin.add((self.B, 512), bf)
+            self._in_layer.append((first, first_attn))
         self._out_layer = [(fout.add((self.B, 64, 512), out_dtype), fout.add((self.B, 64), torch.float32))
                            for _ in range(L)]
         self._fin, self._fout = fin, fout
         self.io_in = torch.zeros(fin.size, dtype=u8, device=d)
         self.io_out = torch.zeros(fout.size, dtype=u8, device=d)
         vin, vout = fin.views(self.io_in), fout.views(self.io_out)
-        self.attn_q = [vin[self._in_layer[li][1][0]] for li in range(L)]
+        self.attn_q = [vin[vid[li, "q"]] for li in range(L)]
         self.out = [vout[o] for o, _ in self._out_layer]
         self.lse = [vout[l_] for _, l_ in self._out_layer]
-        self.iq_bf16 = {i: vin[self._in_layer[i][1][2]] for i in self.index_layers}
+        self.iq_bf16 = {i: vin[vid[i, "iq"]] for i in self.index_layers}
         self.iq_codes = {i: torch.zeros((self.B * 32 * 64,), dtype=u8, device=d) for i in self.index_layers}
         self.iq_scales = {i: torch.zeros((self.B * 32, 8), dtype=u8, device=d) for i in self.index_layers}
-        self.iw = {i: vin[self._in_layer[i][1][3]] for i in self.index_layers}
+        self.iw = {i: vin[vid[i, "iw"]] for i in self.index_layers}
         self.topk = {i: torch.full((self.B, self.K), -1, dtype=torch.int32, device=d) for i in self.index_layers}
         self.pool = torch.full((self.B, self.P), -1, dtype=torch.int32, device=d)
         # current-token inputs of a decode step
         self.tok_latent, self.tok_ik = vin[i_tok[0]], vin[i_tok[1]]
-        self.tok_swa = [vin[self._in_layer[li][1][1]] for li in range(L)]
+        self.tok_swa = [vin[vid[li, "swa"]] for li in range(L)]
         last = self.contexts - 1
         self.tok_pos = torch.from_numpy(last * wl.m + (wl.m - 1)).to(d)
         self.tok_row = torch.from_numpy(starts + last).to(d)
@@ -204,6 +208,11 @@ class LayerGroup:
     def layer(self, li, s, swa_append=True):
         """One layer: index (Full / Reindex; Reuse makes no call), then
         attention with this layer's window append fused in (swa_append)."""
+        self.layer_index(li, s)
+        self.layer_attn(li, s, swa_append)
+
+    def layer_index(self, li, s):
+        """The index part of a layer (Full / Reindex; Reuse makes no call)."""
         mode = self.layers[li]
         B = self.B
         if mode in (W.FULL, W.REINDEX):
@@ -219,6 +228,10 @@ class LayerGroup:
                                    self.ik_scales, self.n_rows, self.kv_start, self.n_visible,
                                    self.max_visible, self.pool, self.P, self.K, self.topk[li], self.ws_re,
                                    self.ws_re.numel(), s)
+
+    def layer_attn(self, li, s, swa_append=True):
+        """The attention of a layer over its index source's top-k."""
+        B = self.B
         src = W.index_source(self.wl, li)
         abi.csa2_sparse_attn(self.attn_q[li], B, self.kv_codes, self.kv_scales, self.n_rows, self.kv_start,
                              self.n_visible, self.topk[src], self.K, self.swa[li],
@@ -256,48 +269,52 @@ class LayerGroup:
         vin, vout = self._fin.views(flat_in), self._fout.views(flat_out)
         app = vin[:2] if not self.wl.shared_cache else []
         layers = []
-        for li, (_, items) in enumerate(self._in_layer):
-            t = [vin[items[0]]] + ([vin[items[1]]] if not self.wl.shared_cache else []) + [vin[i] for i in items[2:]]
-            layers.append(t)
+        for li, (first, first_attn) in enumerate(self._in_layer):
+            t = [vin[first_attn]] + ([vin[first_attn + 1]] if not self.wl.shared_cache else [])
+            layers.append(t + vin[first:first_attn])
         outs = [[vout[o], vout[l_]] for o, l_ in self._out_layer]
         return HostIO(app, layers, outs, flat_in, flat_out)
 
-    # layers before which the compute stream waits for the inputs copied so
-    # far: a wait that breaks the chain of programmatic launches costs a few
-    # microseconds, so the inputs come in a few growing groups
-    IO_WAIT_AT = (0, 1, 3, 7, 15)
+    # where the compute stream waits for the inputs copied so far, as (layer,
+    # part) with part 0 the index calls and 1 the attention: a wait breaks
+    # the chain of programmatic launches and costs a few microseconds, so the
+    # inputs come in a few growing groups, the first one small
+    IO_WAIT_AT = ((0, 0), (0, 1), (3, 0), (8, 0), (15, 0))
 
     def step_io(self, stream, copy_streams, host):
         """step() with its host I/O pipelined on two more streams: the first
         brings the inputs in from pinned host memory in a few growing groups
-        of layers (one copy each, ahead of the group), the second returns
-        each layer's [out, lse] in one copy as soon as that layer is done,
-        while `stream` computes the later layers.  `host` comes from
-        host_buffers()."""
+        (one copy each, ahead of their use), the second returns each layer's
+        [out, lse] in one copy as soon as that layer is done, while `stream`
+        computes the later layers.  `host` comes from host_buffers()."""
         h2d, d2h = copy_streams
         L = len(self.layers)
-        waits = [w for w in self.IO_WAIT_AT if w < L]
-        bounds = waits[1:] + [L]
+        waits = [w for w in self.IO_WAIT_AT if w[0] < L]
+        first_item = lambda w: self._in_layer[w[0]][w[1]]
+        starts = [0] + [self._fin.offset(first_item(w)) for w in waits[1:]]
+        ends = starts[1:] + [self._fin.size]
         start = torch.cuda.Event()
         start.record(stream)
         h2d.wait_event(start)
         d2h.wait_event(start)
-        ev_group = {}
+        ev = {}
         with torch.cuda.stream(h2d):
-            for k, (w0, w1) in enumerate(zip(waits, bounds)):
-                lo = 0 if k == 0 else self._fin.offset(self._in_layer[w0][0])
-                hi = self._fin.offset(self._in_layer[w1][0]) if w1 < L else self._fin.size
+            for w, lo, hi in zip(waits, starts, ends):
                 self.io_in[lo:hi].copy_(host.flat_in[lo:hi], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(h2d)
-                ev_group[w0] = e
-        stream.wait_event(ev_group[0])
+                ev[w] = e
+        stream.wait_event(ev[waits[0]])
         if not self.wl.shared_cache:
             self.append_token(stream)
         for li in range(L):
-            if li in ev_group and li > 0:
-                stream.wait_event(ev_group[li])
-            self.layer(li, stream, swa_append=not self.wl.shared_cache)
+            for part in (0, 1):
+                if (li, part) in ev and (li, part) != waits[0]:
+                    stream.wait_event(ev[li, part])
+                if part == 0:
+                    self.layer_index(li, stream)
+                else:
+                    self.layer_attn(li, stream, swa_append=not self.wl.shared_cache)
             done = torch.cuda.Event()
             done.record(stream)
             d2h.wait_event(done)
