@@ -911,13 +911,15 @@ __device__ void select_regs(const uint32_t (&k)[KPT], int n, int count, int pad_
     uint32_t thr = 0;
     int take_eq = n;  // count == n: every key is taken
     if (count < n) kary_regs<KPT>(k, lo, hi, count, thr, take_eq, sm);
-    int gt = 0, eq = 0;
+    static_assert(KPT <= 32, "one bit per key");
+    uint32_t gt_m = 0, eq_m = 0;  // this thread's keys above / equal to thr
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
         const bool in = KPT * tid + j < n;
-        gt += in && k[j] > thr;
-        eq += in && k[j] == thr;
+        gt_m |= uint32_t(in && k[j] > thr) << j;
+        eq_m |= uint32_t(in && k[j] == thr) << j;
     }
+    const int gt = __popc(gt_m), eq = __popc(eq_m);
     int gi = gt, ei = eq;  // inclusive scans over the lanes
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -963,15 +965,16 @@ __device__ void select_regs(const uint32_t (&k)[KPT], int n, int count, int pad_
         if (lane >= o) si += y;
     }
     int pos = __shfl_sync(0xffffffffu, is - sw, warp) + si - sel;
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-        const bool in = KPT * tid + j < n;
-        bool s = in && k[j] > thr;
-        if (in && k[j] == thr && take > 0) {
-            s = true;
-            --take;
-        }
-        if (s) out[pos++] = map(KPT * tid + j);
+    // the selected keys: all above thr and the first `take` equal to it
+    uint32_t sel_m = gt_m;
+    for (int t = 0; t < take; ++t) {
+        sel_m |= eq_m & (0u - eq_m);  // lowest remaining equal key
+        eq_m &= eq_m - 1u;
+    }
+    while (sel_m) {
+        const int j = __ffs(sel_m) - 1;
+        sel_m &= sel_m - 1u;
+        out[pos++] = map(KPT * tid + j);
     }
     for (int i = count + tid; i < pad_to; i += blockDim.x) out[i] = -1;
 }
