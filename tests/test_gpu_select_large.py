@@ -1,8 +1,14 @@
-"""csa2_index_full on contexts whose block maxima do not fit one CTA's shared
-memory: the pool selection then splits each query's blocks over a cluster of
-CTAs (16K or 32K keys each).  The indexer keys repeat 16 distinct rows, so
-the oracle's scores come from a 16-entry table and exact ties are everywhere,
-including across the cluster's segments."""
+"""csa2_index_full at the size boundaries of the selection paths, with exact
+ties everywhere: the indexer keys repeat 16 distinct rows, so the oracle's
+scores come from a 16-entry table.
+
+- Contexts whose block maxima do not fit one CTA's shared memory: the pool
+  selection splits each query's blocks over a cluster of CTAs (16K or 32K
+  keys each), and the ties run across the cluster's segments.
+- 8192 / 8193 and 16,384 / 16,385 blocks: 8 or 16 keys per thread held in
+  registers, or staged in shared memory.
+- A context of fewer than P blocks: every block is taken, and the pool is
+  padded with -1, so the top-K candidates include missing positions."""
 import numpy as np
 import pytest
 import torch
@@ -13,8 +19,9 @@ from tests.helpers import check_selection, kth_value, rows_to_block8
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("contexts", [(300_000, 50_000, 262_143), (1_600_000, 1_000_003)])
-def test_pool_and_topk_with_cluster_selection(contexts):
+@pytest.mark.parametrize("contexts", [(300_000, 50_000, 262_143), (1_600_000, 1_000_003),
+                                      (65_536, 65_537, 131_072, 131_073, 8_000)])
+def test_pool_and_topk_at_selection_path_boundaries(contexts):
     from csa2_sparse_attention_gb300 import abi
     rng = np.random.default_rng(sum(contexts))
     n_q, P, K = len(contexts), 2048, 512
