@@ -51,7 +51,7 @@ typedef int csa2_status;
 enum {
     CSA2_OK = 0,
     CSA2_ERR_INVALID_ARG = 1,   /* null pointer, misalignment, bad size      */
-    CSA2_ERR_UNSUPPORTED = 2,   /* a shape or format this build does not run  */
+    CSA2_ERR_UNSUPPORTED = 2,   /* a shape or format this library does not run */
     CSA2_ERR_CUDA = 3,          /* a CUDA launch or runtime error             */
     CSA2_ERR_TIMEOUT = 4,       /* device: a bounded wait gave up             */
     CSA2_ERR_DEVICE_BOUNDS = 5, /* device: a row/index outside its bounds was skipped */
