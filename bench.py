@@ -376,6 +376,24 @@ class L2Flush:
         self.r.max()
 
 
+def max_over_ranks(x, device):
+    """The largest x over all ranks of the process group (x itself when the
+    job runs alone): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(batch, world, steps, total_ms):
+    """Whole-job queries/s: every rank runs `steps` steps of its own batch
+    (replicas), timed by the slowest rank's total."""
+    return batch * world * steps / (total_ms / 1000.0)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -430,12 +448,8 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = wl.batch * world * K / (total_ms / 1000.0)
+    total_ms = max_over_ranks(float(sum(step_ms)), dev)
+    value = job_throughput(wl.batch, world, K, total_ms)
 
     # ---- per-kernel device time (eager steps, L2 flushed, events on the launch stream)
     n_prof = max(3, min(20, K))

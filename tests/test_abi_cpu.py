@@ -89,3 +89,21 @@ def test_host_argument_errors_return_before_launch(abi):
     assert st == A.ERR_INVALID_ARG  # unknown output type
     with pytest.raises(A.Csa2Error):
         A.csa2_rope_table_init(10000.0, 512, 0, fake, None)
+
+
+def test_empty_batches_return_ok_and_launch_nothing(abi):
+    """Every call with zero rows or queries returns OK after its argument and
+    workspace checks, touching no memory (the pointers are never valid) and
+    launching nothing."""
+    A = abi
+    fake = 1 << 20
+    c0 = A.csa2_launch_count()
+    assert A.lib.csa2_quantize_append(fake, 0, 512, A.FMT_FP4, A.LAYOUT_ROWS, None, None, 0, None, 4,
+                                      fake, fake, fake, 256, None) == A.OK
+    assert A.lib.csa2_index_full(fake, fake, fake, 0, fake, fake, 16, fake, fake, 100, 2048, 512,
+                                 fake, fake, fake, 1 << 30, None) == A.OK
+    assert A.lib.csa2_index_reindex(fake, fake, fake, 0, fake, fake, 16, fake, fake, 100, fake, 2048, 512,
+                                    fake, fake, 1 << 30, None) == A.OK
+    assert A.lib.csa2_sparse_attn(fake, 0, fake, fake, 16, fake, fake, fake, 512, fake, None, 128, 0.04,
+                                  fake, A.OUT_F32, None, fake, 1 << 30, None) == A.OK
+    assert A.csa2_launch_count() == c0

@@ -194,3 +194,52 @@ def test_step_with_pipelined_host_io_matches_plain_step():
     for li, (o, l) in enumerate(plain):
         assert torch.equal(host[2][li][0], o.cpu()), f"layer {li} output"
         assert torch.equal(host[2][li][1], l.cpu()), f"layer {li} lse"
+
+
+def test_index_calls_with_a_query_that_sees_nothing():
+    """csa2_index_full and csa2_index_reindex where one query of three has no
+    visible position: its pool and top-k are all -1 pads, the other queries
+    match the oracle, and nothing is recorded as an error."""
+    from csa2_sparse_attention_gb300 import abi
+    from tests.helpers import check_selection, kth_value, rows_to_block8
+    contexts = (5000, 0, 300)
+    n_q, P, K = len(contexts), 256, 128
+    rng = np.random.default_rng(31)
+    rows_of = [max(8, ((n + 7) // 8) * 8) for n in contexts]
+    kv_start = np.concatenate([[0], np.cumsum(rows_of)[:-1]]).astype(np.int64)
+    n_rows = int(sum(rows_of))
+    k_real = torch.randn((n_rows, 128), generator=torch.Generator().manual_seed(32)).to(torch.bfloat16)
+    kc, ks = O.quantize_fp4(k_real.float().numpy().astype(np.float64))
+    kdq = O.dequantize_fp4(kc, ks)
+    q_real = torch.randn((n_q * 32, 128), generator=torch.Generator().manual_seed(33)).to(torch.bfloat16)
+    qc, qs = O.quantize_fp4(q_real.float().numpy().astype(np.float64))
+    qdq = O.dequantize_fp4(qc, qs).reshape(n_q, 32, 128)
+    w = rng.uniform(0, 1, (n_q, 32)).astype(np.float32)
+    d = "cuda"
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(d)
+    args = (t(rows_to_block8(O.pack_codes(qc))), t(qs), t(w), n_q, t(rows_to_block8(O.pack_codes(kc))), t(ks),
+            n_rows, t(kv_start), t(np.asarray(contexts, dtype=np.int32)), max(contexts))
+    ws = torch.zeros(abi.csa2_workspace_bytes(abi.OP_INDEX_FULL, n_q, max(contexts), P, K), dtype=torch.uint8,
+                     device=d)
+    pool = torch.full((n_q, P), -7, dtype=torch.int32, device=d)
+    topk = torch.full((n_q, K), -7, dtype=torch.int32, device=d)
+    abi.csa2_index_full(*args, P, K, pool, topk, ws, ws.numel())
+    ws_re = torch.zeros(abi.csa2_workspace_bytes(abi.OP_INDEX_REINDEX, n_q, max(contexts), P, K),
+                        dtype=torch.uint8, device=d)
+    topk_re = torch.full((n_q, K), -7, dtype=torch.int32, device=d)
+    abi.csa2_index_reindex(*args, pool, P, K, topk_re, ws_re, ws_re.numel())
+    torch.cuda.synchronize()
+    assert abi.csa2_status_fetch(ws)[0] == 0 and abi.csa2_status_fetch(ws_re)[0] == 0
+    assert torch.all(pool[1] == -1) and torch.all(topk[1] == -1) and torch.all(topk_re[1] == -1)
+    for q in (0, 2):
+        n = contexts[q]
+        scores = O.index_scores(qdq[q], w[q].astype(np.float64), kdq[kv_start[q]:kv_start[q] + n])
+        bmax = O.block_max(scores)
+        check_selection(pool[q].cpu().numpy(), O.select_top(bmax, P), lambda b: bmax[b], kth_value(bmax, P),
+                        f"q{q} pool")
+        top_o = O.select_top(scores, K)
+        check_selection(topk[q].cpu().numpy(), top_o, lambda p: scores[p], kth_value(scores, K), f"q{q} top-k")
+        re_o, cand, sc = O.index_reindex(qdq[q], w[q].astype(np.float64), kdq[kv_start[q]:kv_start[q] + n], n,
+                                         pool[q].cpu().numpy(), K)
+        smap = dict(zip(cand.tolist(), sc.tolist()))
+        check_selection(topk_re[q].cpu().numpy(), re_o, lambda p: smap[p], kth_value(sc, K), f"q{q} reindex")
