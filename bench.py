@@ -116,6 +116,9 @@ class ClockSampler:
 MQ_MIN_QUERIES = 256
 # nominal dense FP4 : bf16 tensor throughput (13.5 : 2.25 PFLOP/s)
 FP4_PER_BF16 = 6.0
+# Smaller batches whose candidate pool has at most this many blocks keep the
+# scan's per-position scores for the Full layer's top-K.
+POS_SCORE_MAX_CAND = 2048
 
 
 def alg_flops_per_launch(kernel, g):
@@ -135,14 +138,16 @@ def alg_bytes_per_launch(kernel, g):
     n = np.asarray(g.contexts, dtype=np.int64)
     B, P, K, Wn = g.B, g.P, g.K, g.Wn
     nb = (n + 7) // 8
-    if kernel == "scan_blockmax":   # indexer K stream + block maxima + indexer Q
-        return float(np.sum(n * 72 + nb * 4) + B * 32 * 72)
+    decode_scan = B < MQ_MIN_QUERIES and max(P, K) <= POS_SCORE_MAX_CAND
+    if kernel == "scan_blockmax":   # indexer K stream + block maxima (+ per-position scores) + indexer Q
+        return float(np.sum(n * 72 + nb * 4 + (n * 4 if decode_scan else 0)) + B * 32 * 72)
     if kernel == "attn_split":      # selected FP4 latents + FP8 window + bf16 Q
         return float(np.sum(288 * np.minimum(K, n) + 512 * np.minimum(Wn, n)) + B * 64 * 512 * 2)
     if kernel == "attn_merge":      # bf16 output + lse
         return float(B * (64 * 512 * 2 + 64 * 4))
     if kernel == "pool_score":      # gathered pool blocks (8 rows x 72 B)
-        n_full = sum(1 for m in g.layers if m == W.FULL)
+        # a decode batch's Full layer reads its candidates' scores from the scan instead
+        n_full = 0 if decode_scan else sum(1 for m in g.layers if m == W.FULL)
         n_re = sum(1 for m in g.layers if m == W.REINDEX)
         c_full, c_re = max(P, K), P
         per = [float(np.sum(np.minimum(8 * c_full, nb * 8) * 72))] * n_full + \

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const uint8_t* __restrict__ k_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, const int32_t* __restrict__ cand,
     int64_t cand_stride, int C, float* __restrict__ out, int64_t out_stride, int ctas_per_query,
-    bool check_cand, Status* st) {
+    bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride) {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
     grid_dep_wait();
@@ -366,6 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
             const int64_t t = t0 + i;
             if (!GATHER) {
                 const int64_t pos = t * kTile + row;
+                if (pos_scores != nullptr && pos < n) pos_scores[q * pos_stride + pos] = x;
                 float m = pos < n ? x : -INFINITY;
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
@@ -1120,7 +1121,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ cand,
     int64_t cand_stride, int C, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, int64_t n_rows, int count,
-    int32_t* __restrict__ out, int64_t out_stride, int smem_keys_cap) {
+    int32_t* __restrict__ out, int64_t out_stride, int smem_keys_cap, const float* __restrict__ pos_scores,
+    int64_t pos_stride) {
     extern __shared__ uint32_t smem_dyn[];
     __shared__ SelShared sm;
     int32_t* cblk = reinterpret_cast<int32_t*>(smem_dyn);
@@ -1139,12 +1141,44 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(
         // candidate ids (at most 2 per thread) are only staged in shared
         // memory for the output
         uint32_t k[KR];
-        load_keys<KR>(v, m, k);
         int32_t cid[2];
+        if (pos_scores == nullptr) {
+            load_keys<KR>(v, m, k);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int i = int(threadIdx.x) + r * kSelThreads;
-            cid[r] = i < C ? cq[i] : -1;
+            for (int r = 0; r < 2; ++r) {
+                const int i = int(threadIdx.x) + r * kSelThreads;
+                cid[r] = i < C ? cq[i] : -1;
+            }
+        } else {
+            // keys 16t .. 16t + 15 are the 8 positions of candidates 2t and
+            // 2t + 1, read from the scan's per-position scores (rows 16-byte
+            // aligned); missing positions score -inf as the pool scorer's do
+            const int32_t n = checked_visible(kv_start, n_visible, q, max_visible, n_rows, nullptr, false);
+            const int nb = (n + 7) >> 3;
+            const float* ps = pos_scores + q * pos_stride;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int ci = 2 * int(threadIdx.x) + r;
+                const int32_t b = ci < C ? cq[ci] : -1;
+                float x[8];
+                if (b >= 0 && b < nb) {
+                    const float4 lo = reinterpret_cast<const float4*>(ps + 8 * int64_t(b))[0];
+                    const float4 hi = reinterpret_cast<const float4*>(ps + 8 * int64_t(b))[1];
+                    x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+                    x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[j] = -INFINITY;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    k[8 * r + j] = float_key(b >= 0 && b < nb && 8 * b + j < n ? x[j] : -INFINITY);
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i = int(threadIdx.x) + r * kSelThreads;
+                cid[r] = i < C ? cq[i] : -1;
+            }
         }
         for (int i = threadIdx.x; i < kSelWarps * 33; i += blockDim.x) (&sm.tbins[0][0])[i] = 0;
         select_regs<KR, true>(k, m, count, count, out + q * out_stride, CandPosMap{cblk}, sm, [&] {
@@ -1204,7 +1238,6 @@ constexpr int kMqThreads = 64 + kMqQ * 128;
 constexpr int kMqAcc = 2;                         // accumulators (128 TMEM columns each)
 constexpr uint32_t kMqCols = 512;
 constexpr uint32_t kMqColSfa = 256, kMqColSfb = 288;  // scale slots (4 x 8 columns), query scales (8)
-constexpr int kMqMinQueries = 256;  // batches at least this large use this scan
 
 struct MqSmem {
     uint8_t codes[kTcStages][kTile * 64];
@@ -1504,19 +1537,24 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
                              const uint8_t* k_codes, const uint8_t* k_scales, int64_t n_rows,
                              const int64_t* kv_start, const int32_t* n_visible, int32_t max_visible,
                              const int32_t* cand, int64_t cand_stride, int C, int topk, int32_t* out_topk,
-                             float* scores, int64_t score_stride, bool check_cand, Status* st, cudaStream_t s) {
-    const int64_t cpq = tc_ctas_per_query(n_q, (C + 15) / 16);
-    const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
-    timer_begin(K_POOL_SCORE, s);
-    launch(score_tc_kernel<true>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
-        q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand, cand_stride, C,
-        scores, score_stride, int(cpq), check_cand, st);
-    timer_end(K_POOL_SCORE, s);
+                             float* scores, int64_t score_stride, bool check_cand, Status* st, cudaStream_t s,
+                             const float* pos_scores = nullptr, int64_t pos_stride = 0) {
+    // with the scan's per-position scores at hand (pos_scores), the candidates
+    // are not scored again: the selection reads their scores from there
+    if (pos_scores == nullptr) {
+        const int64_t cpq = tc_ctas_per_query(n_q, (C + 15) / 16);
+        const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
+        timer_begin(K_POOL_SCORE, s);
+        launch(score_tc_kernel<true>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
+            q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand, cand_stride, C,
+            scores, score_stride, int(cpq), check_cand, st, nullptr, int64_t(0));
+        timer_end(K_POOL_SCORE, s);
+    }
     const int cap_t = sel_cap(8 * int64_t(C));
     timer_begin(K_SELECT_TOPK, s);
     launch(select_topk_kernel, unsigned(n_q), kSelThreads, size_t(cap_t + C) * 4, s, 1,
         scores, score_stride, cand, cand_stride, C, kv_start, n_visible, max_visible, n_rows, topk, out_topk, topk,
-        cap_t);
+        cap_t, pos_scores, pos_stride);
     timer_end(K_SELECT_TOPK, s);
 }
 
@@ -1562,7 +1600,8 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         timer_begin(K_SCAN, s);
         launch(score_tc_kernel<false>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0,
-            n_q <= kScanMaxQ ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st);
+            n_q <= kScanMaxQ ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st,
+            L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride);
         timer_end(K_SCAN, s);
     }
     launch_select_blocks(blockmax, L.nb_stride, n_q, kv_start, n_visible, max_visible, n_rows, pool_blocks,
@@ -1578,7 +1617,9 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         cand_stride = topk;
     }
     launch_pool_topk(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand,
-                     cand_stride, C, topk, out_topk, scores, L.score_stride, false, st, s);
+                     cand_stride, C, topk, out_topk, scores, L.score_stride, false, st, s,
+                     L.pos_stride && max_visible > 0 ? reinterpret_cast<const float*>(base + L.pos) : nullptr,
+                     L.pos_stride);
     return launch_status();
 }
 

@@ -17,9 +17,17 @@ __host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~si
 
 // csa2_index_full: block maxima, the wide candidate list (only when
 // topk > pool_blocks), and per-candidate-position scores.
+// Batches of at least this many queries run the full scan as the many-query
+// contraction (groups of queries share each K tile).
+constexpr int64_t kMqMinQueries = 256;
+// Smaller batches whose candidate pool has at most this many blocks keep the
+// scan's per-position scores, and the Full layer's top-K reads them instead
+// of scoring the pool again.
+constexpr int64_t kPosScoreMaxCand = 2048;
+
 struct IndexFullWs {
-    size_t blockmax, cand, scores, total;
-    int64_t nb_stride, cand_stride, score_stride;
+    size_t blockmax, cand, scores, pos, total;
+    int64_t nb_stride, cand_stride, score_stride, pos_stride;  // pos_stride 0: no per-position scores
 };
 __host__ __device__ inline IndexFullWs index_full_ws(int64_t n_q, int64_t max_visible, int P, int K) {
     IndexFullWs w{};
@@ -27,13 +35,16 @@ __host__ __device__ inline IndexFullWs index_full_ws(int64_t n_q, int64_t max_vi
     const int64_t C = P > K ? P : K;
     w.cand_stride = C;
     w.score_stride = 8 * C;
+    w.pos_stride = (n_q < kMqMinQueries && C <= kPosScoreMaxCand) ? 8 * w.nb_stride : 0;
     size_t off = CSA2_STATUS_BYTES;
     w.blockmax = off;
     off = align256(off + size_t(n_q) * size_t(w.nb_stride) * 4);
     w.cand = off;
     if (K > P) off = align256(off + size_t(n_q) * size_t(C) * 4);
     w.scores = off;
-    off = align256(off + size_t(n_q) * size_t(w.score_stride) * 4);
+    if (w.pos_stride == 0) off = align256(off + size_t(n_q) * size_t(w.score_stride) * 4);
+    w.pos = off;
+    off = align256(off + size_t(n_q) * size_t(w.pos_stride) * 4);
     w.total = off;
     return w;
 }
