@@ -129,6 +129,9 @@ class LayerGroup:
         self.iw = {i: vin[vid[i, "iw"]] for i in self.index_layers}
         self.topk = {i: torch.full((self.B, self.K), -1, dtype=torch.int32, device=d) for i in self.index_layers}
         self.pool = torch.full((self.B, self.P), -1, dtype=torch.int32, device=d)
+        # per layer, the top-k tensor its attention call was given (Reuse
+        # layers get their index source's buffer itself, not a copy)
+        self.attn_index = {}
         # current-token inputs of a decode step
         self.tok_latent, self.tok_ik = vin[i_tok[0]], vin[i_tok[1]]
         self.tok_swa = [vin[vid[li, "swa"]] for li in range(L)]
@@ -232,9 +235,10 @@ class LayerGroup:
     def layer_attn(self, li, s, swa_append=True):
         """The attention of a layer over its index source's top-k."""
         B = self.B
-        src = W.index_source(self.wl, li)
+        idx = self.topk[W.index_source(self.wl, li)]
+        self.attn_index[li] = idx
         abi.csa2_sparse_attn(self.attn_q[li], B, self.kv_codes, self.kv_scales, self.n_rows, self.kv_start,
-                             self.n_visible, self.topk[src], self.K, self.swa[li],
+                             self.n_visible, idx, self.K, self.swa[li],
                              self.tok_swa[li] if swa_append else None, self.Wn, self.sm_scale,
                              self.out[li], self.out_code, self.lse[li], self.ws_attn, self.ws_attn.numel(), s)
 

@@ -34,9 +34,12 @@ def rows_to_block8(rows):
     return np.ascontiguousarray(rows.reshape(n // 8, 8, 4, 16).transpose(0, 2, 1, 3)).reshape(-1)
 
 
-def check_selection(gpu_ids, oracle_ids, score_of, kth, label=""):
+def check_selection(gpu_ids, oracle_ids, score_of, kth, label="", strict=False):
     """Sets equal except members whose score is within TOPK_REL of kth.
-    gpu_ids must be ascending then -1 padded."""
+    gpu_ids must be ascending then -1 padded.  strict: the sets must be
+    exactly equal (no waiver), for inputs whose scores are exact on both
+    sides, so that equal scores are genuine ties the rule breaks toward the
+    lower index."""
     g = np.asarray(gpu_ids)
     valid = g[g >= 0]
     assert np.all(g[len(valid):] == -1), f"{label}: pads not at the end"
@@ -45,6 +48,9 @@ def check_selection(gpu_ids, oracle_ids, score_of, kth, label=""):
     o = o[o >= 0]
     assert len(valid) == len(o), f"{label}: {len(valid)} vs {len(o)} selected"
     diff = set(valid.tolist()) ^ set(o.tolist())
+    if strict:
+        assert not diff, f"{label}: {len(diff)} members differ (strict), e.g. {sorted(diff)[:5]}"
+        return 0
     tol = TOPK_REL * max(abs(kth), 1e-30)
     bad = [p for p in diff if abs(score_of(p) - kth) > tol]
     assert not bad, f"{label}: {len(bad)} members differ beyond tolerance, e.g. {bad[:5]}"

@@ -24,8 +24,11 @@ def test_tiny_group_8k():
     g = run_group(wl)
     check_status(g)
     verify_query(g, wl, 0)
-    # Reuse layer 2 attends over exactly the Reindex layer's indices
-    assert g.topk[1].data_ptr() == g.topk[1].data_ptr()
+    # the Reuse layer attends over the Reindex layer's own top-k buffer (the
+    # same device memory, not a copy); only Full/Reindex layers own one
+    assert sorted(g.topk) == [0, 1]
+    assert g.attn_index[2] is g.topk[1] and g.attn_index[2].data_ptr() == g.topk[1].data_ptr()
+    assert g.attn_index[1] is g.topk[1] and g.attn_index[0] is g.topk[0]
 
 
 @pytest.mark.parametrize("pool,topk", [(2048, 512), (256, 512), (64, 100)])

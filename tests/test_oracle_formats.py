@@ -158,3 +158,41 @@ def test_dequantize_roundtrip_is_exact_on_representable_values():
     same_scale = (s2 == scales)
     g = np.repeat(same_scale, 16, axis=1)
     assert np.array_equal(v[g], v2[g])
+
+
+def test_dequantize_fp4_hand_values_one_scale_per_16_channels():
+    """Hand-computed products: channel c takes code c's E2M1 value times the
+    E4M3 scale of group c // 16.  The groups carry different scales (0.5 and
+    6.0; 448 and the subnormal 3 * 2^-9), so a scale applied to the wrong
+    channels, a dropped sign or a mis-decoded scale changes the values."""
+    codes = np.array([
+        list(range(16)) + [7, 6, 5, 4, 3, 2, 1, 0, 15, 14, 13, 12, 11, 10, 9, 8],
+        [7, 7, 7, 1] + [7] * 12 + [7, 9] + [0] * 14,
+    ])
+    scales = np.array([[0x30, 0x4C], [0x7E, 0x03]], dtype=np.uint8)  # 0.5, 6.0; 448, 3/512
+    expect = np.array([
+        [0, 0.25, 0.5, 0.75, 1, 1.5, 2, 3, -0.0, -0.25, -0.5, -0.75, -1, -1.5, -2, -3,
+         36, 24, 18, 12, 9, 6, 3, 0, -36, -24, -18, -12, -9, -6, -3, -0.0],
+        [2688, 2688, 2688, 224] + [2688] * 12 + [0.03515625, -0.0029296875] + [0] * 14,
+    ])
+    got = O.dequantize_fp4(codes, scales)
+    assert np.array_equal(got, expect)
+    assert np.array_equal(np.signbit(got), np.signbit(expect))  # code 8 is -0
+
+
+def test_strict_selection_check_catches_ties_broken_upward():
+    """The strict set check used on tie-heavy GPU inputs is not vacuous: a
+    selection that breaks ties toward the higher index passes the tolerant
+    check (the differing members score exactly the K-th value) but fails the
+    strict one."""
+    from tests.helpers import check_selection, kth_value
+    vals = np.array([5.0, 3.0, 3.0, 3.0, 1.0, 3.0])
+    good = O.select_top(vals, 3)                    # 0, 1, 2
+    order = np.lexsort((-np.arange(vals.size), -vals))  # ties toward the higher index
+    upward = np.sort(order[:3])                     # 0, 3, 5
+    assert good.tolist() == [0, 1, 2] and upward.tolist() == [0, 3, 5]
+    kth = kth_value(vals, 3)
+    check_selection(upward, good, lambda p: vals[p], kth, "tolerant")
+    with pytest.raises(AssertionError):
+        check_selection(upward, good, lambda p: vals[p], kth, "strict", strict=True)
+    check_selection(good, good, lambda p: vals[p], kth, "strict", strict=True)
