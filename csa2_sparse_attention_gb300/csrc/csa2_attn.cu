@@ -13,11 +13,14 @@
 // times its E4M3 scale and every E4M3 value is exact in f16), converts Q to
 // f16 with a per-query power-of-two scale (exact except for elements far
 // below max|Q|), computes S^T = C Q^T with one tcgen05 MMA chain (M = 128
-// entries, N = 64 heads, K = 512, fp32 accumulate in TMEM), stages S through
-// shared memory for the split's softmax statistics (m, l), and computes
-// O^T = C^T P^T (M = 4 x 128 dims, N = 64 heads, K = 128 entries) with P
-// split into f16 hi + lo parts (the partial output carries ~2^-21 relative
-// error from P).  One shared-memory copy of C serves both products: K-major
+// entries, N = 64 heads, K = 512, fp32 accumulate in TMEM), takes the
+// split's softmax statistics (m, l) from registers (a transposing warp
+// reduction), and computes O^T = C^T P^T (M = 4 x 128 dims, K = 128
+// entries) with P split into f16 hi + lo parts side by side as one N = 128
+// operand: on this tensor core an M = 128 MMA takes the same time at
+// N = 128 as at N = 64, so the lo part costs no extra MMAs (the partial
+// output carries ~2^-21 relative error from P).  One shared-memory copy of
+// C serves both products: K-major
 // for the first, MN-major for the second.  The splits of a query form one
 // thread-block cluster when all clusters of the launch can be resident
 // together: each CTA parks its fp32 partial in its own shared memory and
@@ -44,10 +47,10 @@ constexpr int kH = CSA2_ATTN_HEADS;
 constexpr int kD = CSA2_LATENT_DIM;
 
 constexpr int kTcE = 128;          // entries per CTA = M of S^T
-constexpr uint32_t kTcCols = 512;  // TMEM columns: S^T (64) + O^T (4 x 64)
+constexpr uint32_t kTcCols = 512;  // TMEM columns: S^T [0, 64); then O^T, 4 blocks of 128 (the first over S^T)
 
 struct AttnTcSmem {
-    uint8_t r0[64 * 1024];         // Q f16 (B of S^T); then S fp32 [64][128] + P hi/lo f16
+    uint8_t r0[64 * 1024];         // Q f16 (B of S^T); then P^T hi/lo f16 [0, 32K) and softmax partials
     uint8_t c[kTcE * 1024];        // C [128 entries][512] f16; then the fp32 partial (cluster merge)
     int ok[kTcE];                  // entry valid
     uint32_t qmax[kAttnThreads / 32];  // per-warp max |Q| (bf16 magnitude bits)
@@ -59,12 +62,12 @@ struct AttnTcSmem {
 // canonical no-swizzle K-major offsets: rows of 512 16-bit elements, 16-byte
 // chunk c of row r -> (r/8)*8192 + c*128 + (r%8)*16
 __device__ __forceinline__ uint32_t row512(int r, int c) { return uint32_t((r >> 3) * 8192 + c * 128 + (r & 7) * 16); }
-// P [64 heads][128 entries] bf16, K-major
-__device__ __forceinline__ uint32_t poff(int h, int e) {
-    return uint32_t((h >> 3) * 2048 + (e >> 3) * 128 + (h & 7) * 16 + (e & 7) * 2);
+// P^T [128 entries][128] f16, MN-major B operand of O^T: 8-entry groups of
+// 2 KB, 8-column chunks of 128 B; column n < 64 is head n's hi part, 64 + n
+// its lo part.
+__device__ __forceinline__ uint32_t pmn(int e, int n) {
+    return uint32_t((e >> 3) * 2048 + (n >> 3) * 128 + (e & 7) * 16 + (n & 7) * 2);
 }
-// S [64 heads][128 entries] fp32 with the entry index XOR-swizzled by head
-__device__ __forceinline__ int soff(int h, int e) { return h * kTcE + (e ^ ((h & 7) << 2)); }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -318,53 +321,93 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
                        kk > 0);
         tc_commit(&S.bar);
     }
-    bool ok_mma = mbar_wait(&S.bar, 0);
+    // ok_mma: the MMAs issued so far are done.  A wait that gives up leaves
+    // them in flight: the CTA then writes nothing more into C or the Q/P
+    // area (their operands), takes part in the cluster barriers only, and
+    // waits for them once more before TMEM is released.
+    bool ok_mma = __syncthreads_and(mbar_wait(&S.bar, 0));
+    uint32_t pending = ok_mma ? 0u : 1u;  // 1 + the parity of the MMA commit still outstanding
     tc_fence_after();
-    float* Ssm = reinterpret_cast<float*>(S.r0);  // Q is consumed: reuse for S
-    if (ok_mma) {  // warp -> lanes 32*(warp%4).. (entries), heads 32*(warp/4)..
-        uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + 32 * (warp >> 2), r);
-        tmem_ld_wait();
-        const int e = 32 * (warp & 3) + lane;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) Ssm[soff(32 * (warp >> 2) + j, e)] = __uint_as_float(r[j]);
-    }
-    __syncthreads();
 
-    // softmax statistics: thread -> (head tid/4, entries c0, c0+4, ...)
-    uint8_t* p_hi = S.r0 + 32 * 1024;
-    uint8_t* p_lo = S.r0 + 48 * 1024;
-    {
-        constexpr int PER = kTcE / 4;
-        const int h = tid >> 2, c0 = tid & 3;
-        float x[PER], m = -INFINITY;
+    // softmax statistics from the registers: warp -> entries 32 (warp % 4) +
+    // lane, heads 32 (warp / 4) + j.  P^T (f16 hi for heads 0..63, lo for
+    // heads 64..127 of a 128-column B operand) goes to the consumed Q area.
+    uint8_t* pt = S.r0;
+    float(*red)[kH] = reinterpret_cast<float(*)[kH]>(S.r0 + 32 * 1024);  // per lane quadrant, per head
+    const int qd = warp & 3, hf = warp >> 2, e = 32 * qd + lane;
+    if (ok_mma) {
+        float x[32];
+        {
+            uint32_t r[32];
+            tmem_ld32(tmem + (uint32_t(32 * qd) << 16) + 32 * hf, r);
+            tmem_ld_wait();
+            const bool oke = S.ok[e];
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int e = c0 + 4 * j;
-            x[j] = S.ok[e] ? sm_eff * Ssm[soff(h, e)] : -INFINITY;
-            m = fmaxf(m, x[j]);
+            for (int j = 0; j < 32; ++j) x[j] = oke ? sm_eff * __uint_as_float(r[j]) : -INFINITY;
         }
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        float l = 0.f;
+        // transpose-reduce: in the round with offset o each lane keeps half
+        // of its values and takes the partner's matching half, so lane l
+        // ends with head 32 hf + l
+        auto reduce = [&](float(&v)[32], bool is_max) {
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int e = c0 + 4 * j;
-            const float p = x[j] == -INFINITY ? 0.f : __expf(x[j] - m);
-            l += p;
-            const __half hi = __float2half_rn(p);
-            *reinterpret_cast<__half*>(p_hi + poff(h, e)) = hi;
-            *reinterpret_cast<__half*>(p_lo + poff(h, e)) = __float2half_rn(p - __half2float(hi));
+            for (int o = 16; o >= 1; o >>= 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < o; ++i) {
+                    const float send = up ? v[i] : v[i + o];
+                    const float keep = up ? v[i + o] : v[i];
+                    const float got = __shfl_xor_sync(0xffffffffu, send, o);
+                    v[i] = is_max ? fmaxf(keep, got) : keep + got;
+                }
+            }
+            return v[0];
+        };
+        {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = x[j];
+            red[qd][32 * hf + lane] = reduce(v, true);
         }
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        if (c0 == 0) {
+        __syncthreads();
+        const int hl = 32 * hf + lane;
+        const float mh = fmaxf(fmaxf(red[0][hl], red[1][hl]), fmaxf(red[2][hl], red[3][hl]));  // this split's max
+        float lh;
+        {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float m = __shfl_sync(0xffffffffu, mh, j);
+                x[j] = x[j] == -INFINITY ? 0.f : __expf(x[j] - m);
+                v[j] = x[j];
+            }
+            lh = reduce(v, false);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // P^T hi and lo, 8 heads per 16-byte store
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float a = x[8 * c + 2 * t], b = x[8 * c + 2 * t + 1];
+                const __half2 h2 = __floats2half2_rn(a, b);
+                const float2 hb = __half22float2(h2);
+                const __half2 l2 = __floats2half2_rn(a - hb.x, b - hb.y);
+                hi[t] = *reinterpret_cast<const uint32_t*>(&h2);
+                lo[t] = *reinterpret_cast<const uint32_t*>(&l2);
+            }
+            *reinterpret_cast<uint4*>(pt + pmn(e, 32 * hf + 8 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(pt + pmn(e, 64 + 32 * hf + 8 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        __syncthreads();  // every read of the maxima is done
+        red[qd][hl] = lh;
+        __syncthreads();
+        if (qd == 0) {  // (m, l) of head hl
+            const float l = red[0][hl] + red[1][hl] + red[2][hl] + red[3][hl];
             if (CLUSTER) {
-                S.ml[h][0] = m;
-                S.ml[h][1] = l;
+                S.ml[hl][0] = mh;
+                S.ml[hl][1] = l;
             } else {
-                float* ml = part_ml + ((q * splits + split) * kH + h) * 2;
-                ml[0] = m;
+                float* ml = part_ml + ((q * splits + split) * kH + hl) * 2;
+                ml[0] = mh;
                 ml[1] = l;
             }
         }
@@ -374,22 +417,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     __syncthreads();
     tc_fence_after();
 
-    // O^T = C^T P^T: 4 blocks of 128 dims; C is the MN-major A operand
+    // O^T = C^T P^T: 4 blocks of 128 dims (C is the MN-major A operand), each
+    // into 128 TMEM columns: heads' hi parts, then their lo parts (an M = 128
+    // MMA costs the same at N = 128 as at N = 64).  Block 0 overwrites S^T,
+    // which has been read.
     if (tid == 0 && ok_mma) {
-        constexpr uint32_t id = idesc_f16(128, 64, 0, true, false);
-        const uint32_t ph = smem_addr(p_hi), pl = smem_addr(p_lo);
+        constexpr uint32_t id = idesc_f16(128, 128, 0, true, true);
+        const uint32_t pb = smem_addr(pt);
         for (int mb = 0; mb < 4; ++mb) {
-            const uint32_t d = tmem + 64 + 64 * mb;
+            const uint32_t d = tmem + 128 * mb;
             for (int kk = 0; kk < kTcE / 16; ++kk)
-                mma_f16_ss(d, umma_desc(sm_c + mb * 2048 + kk * 16384, 8192, 128), umma_desc(ph + kk * 256, 128, 2048),
+                mma_f16_ss(d, umma_desc(sm_c + mb * 2048 + kk * 16384, 8192, 128), umma_desc(pb + kk * 4096, 2048, 128),
                            id, kk > 0);
-            for (int kk = 0; kk < kTcE / 16; ++kk)
-                mma_f16_ss(d, umma_desc(sm_c + mb * 2048 + kk * 16384, 8192, 128), umma_desc(pl + kk * 256, 128, 2048),
-                           id, true);
         }
         tc_commit(&S.bar);
     }
-    if (ok_mma) ok_mma = mbar_wait(&S.bar, 1);
+    if (ok_mma) {
+        ok_mma = __syncthreads_and(mbar_wait(&S.bar, 1));
+        if (!ok_mma) pending = 2u;
+    }
     tc_fence_after();
     // warp -> dims 32*(warp%4) + lane of blocks 2*(warp/4), +1: to the
     // workspace, or (CLUSTER) to this CTA's shared memory (C is consumed)
@@ -400,11 +446,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             const int dim = mb * 128 + 32 * (warp & 3) + lane;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
-                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + 64 + 64 * mb + 32 * half, r);
+                uint32_t rh[32], rl[32];
+                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + 128 * mb + 32 * half, rh);
+                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + 128 * mb + 64 + 32 * half, rl);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) X[(32 * half + j) * kD + dim] = __uint_as_float(r[j]);
+                for (int j = 0; j < 32; ++j)
+                    X[(32 * half + j) * kD + dim] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
             }
         }
     } else if (tid == 0) {
@@ -416,7 +464,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         cluster.sync();  // every partial and (m, l) of the query is visible
         const int rank = int(cluster.block_rank());
         float(*wts)[8] = reinterpret_cast<float(*)[8]>(S.r0);  // P is consumed: merge weights a_s / L
-        if (tid < kH) {  // merge weights of head tid
+        if (pending == 0 && tid < kH) {  // merge weights of head tid
             float mp[8], lp[8], M = -INFINITY;
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
@@ -449,7 +497,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 #pragma unroll
         for (int p = 0; p < 8; ++p)
             px[p] = reinterpret_cast<const float4*>(cluster.map_shared_rank(X, p < splits ? p : 0));
-        for (int idx = tid; idx < kH * w4; idx += kAttnThreads) {
+        for (int idx = tid; pending == 0 && idx < kH * w4; idx += kAttnThreads) {
             const int h = idx / w4, d4 = lo / 4 + idx % w4;
             float4 v[8];
 #pragma unroll
@@ -475,6 +523,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         }
         cluster.sync();  // peers are done reading this CTA's shared memory
     }
+    if (tid == 0 && pending != 0) mbar_wait(&S.bar, pending - 1, 100000000ull);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTcCols);
