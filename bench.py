@@ -322,8 +322,8 @@ def run_append(args):
     pos = torch.from_numpy(W.latent_positions(wl, 0)[:n]).to(dev)
     codes = torch.empty((n, 256), dtype=torch.uint8, device=dev)
     scales = torch.empty((n, 32), dtype=torch.uint8, device=dev)
-    ik_codes = torch.empty(n * 64, dtype=torch.uint8, device=dev)
-    ik_scales = torch.empty((n, 8), dtype=torch.uint8, device=dev)
+    ik_codes = torch.empty(n // 8 * 576, dtype=torch.uint8, device=dev)  # 576-byte records (codes + scales)
+    ik_scales = None
     table = torch.empty(abi.csa2_rope_table_bytes(512, n), dtype=torch.uint8, device=dev)
     ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
@@ -332,7 +332,7 @@ def run_append(args):
     def step():
         abi.csa2_quantize_append(lat, n, 512, abi.FMT_FP4, abi.LAYOUT_ROWS, pos, table, n, None, n,
                                  codes, scales, ws, ws.numel(), stream)
-        abi.csa2_quantize_append(ik, n, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0, None, n,
+        abi.csa2_quantize_append(ik, n, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8R, None, None, 0, None, n,
                                  ik_codes, ik_scales, ws, ws.numel(), stream)
 
     with torch.cuda.stream(stream):
@@ -363,7 +363,7 @@ def run_append(args):
         return 1000 * e0.elapsed_time(e1) / 10
     main_us = alone(lambda: abi.csa2_quantize_append(lat, n, 512, abi.FMT_FP4, abi.LAYOUT_ROWS, pos, table, n, None, n,
                                                      codes, scales, ws, ws.numel(), stream))
-    ik_us = alone(lambda: abi.csa2_quantize_append(ik, n, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0, None, n,
+    ik_us = alone(lambda: abi.csa2_quantize_append(ik, n, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8R, None, None, 0, None, n,
                                                    ik_codes, ik_scales, ws, ws.numel(), stream))
     st = abi.csa2_status_fetch(ws)
     if st[0] != 0:

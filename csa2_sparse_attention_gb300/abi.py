@@ -20,7 +20,7 @@ LIB_PATH = _LIB_PATH
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_BOUNDS, ERR_WORKSPACE = range(7)
 FMT_FP4, FMT_FP8 = 0, 1
-LAYOUT_ROWS, LAYOUT_BLOCK8 = 0, 1
+LAYOUT_ROWS, LAYOUT_BLOCK8, LAYOUT_BLOCK8R = 0, 1, 2
 OP_APPEND, OP_INDEX_FULL, OP_INDEX_REINDEX, OP_SPARSE_ATTN = range(4)
 OUT_BF16, OUT_F32 = 0, 1
 INDEX_HEADS, INDEX_DIM, ATTN_HEADS, LATENT_DIM, BLOCK, STATUS_BYTES = 32, 128, 64, 512, 8, 256

@@ -83,8 +83,10 @@ __device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi) {
     return r & 0xFF;
 }
 
-// FP4 append.  TPR = dim/16 threads per row.
-template <int DIM, bool BLOCK8>
+// FP4 append.  TPR = dim/16 threads per row.  LAYOUT: CSA2_LAYOUT_ROWS,
+// CSA2_LAYOUT_BLOCK8 (scales in their own plane) or CSA2_LAYOUT_BLOCK8R
+// (576-byte records: a block's codes, then its scales; `scales` unused).
+template <int DIM, int LAYOUT>
 __global__ void __launch_bounds__(256, 3) quantize_fp4_kernel(
     const uint4* __restrict__ x, int64_t n, const int64_t* __restrict__ pos,
     const float2* __restrict__ table, int n_hi, int64_t max_pos,
@@ -210,12 +212,17 @@ __global__ void __launch_bounds__(256, 3) quantize_fp4_kernel(
             }
         }
         int64_t off;
-        if (BLOCK8)
+        if (LAYOUT == CSA2_LAYOUT_BLOCK8R)
+            off = (row >> 3) * 576 + (g >> 1) * 128 + (row & 7) * 16 + (g & 1) * 8;
+        else if (LAYOUT == CSA2_LAYOUT_BLOCK8)
             off = (row >> 3) * 512 + (g >> 1) * 128 + (row & 7) * 16 + (g & 1) * 8;
         else
             off = row * (DIM / 2) + 8 * g;
         *reinterpret_cast<uint2*>(codes + off) = make_uint2(cw[0], cw[1]);
-        scales[row * (DIM / 16) + g] = uint8_t(sb);
+        if (LAYOUT == CSA2_LAYOUT_BLOCK8R)
+            codes[(row >> 3) * 576 + 512 + (row & 7) * 8 + g] = uint8_t(sb);
+        else
+            scales[row * (DIM / 16) + g] = uint8_t(sb);
     }
 }
 
@@ -310,9 +317,10 @@ extern "C" csa2_status csa2_quantize_append(const void* x_bf16, int64_t n, int d
         return launch_status();
     }
     if (fmt != CSA2_FMT_FP4) return CSA2_ERR_UNSUPPORTED;
-    if (!dst_scales) return CSA2_ERR_INVALID_ARG;
-    if (layout == CSA2_LAYOUT_BLOCK8 && (dim != 128 || n_rows % 8)) return CSA2_ERR_UNSUPPORTED;
-    if (layout != CSA2_LAYOUT_ROWS && layout != CSA2_LAYOUT_BLOCK8) return CSA2_ERR_UNSUPPORTED;
+    if (layout != CSA2_LAYOUT_ROWS && layout != CSA2_LAYOUT_BLOCK8 && layout != CSA2_LAYOUT_BLOCK8R)
+        return CSA2_ERR_UNSUPPORTED;
+    if (layout == CSA2_LAYOUT_BLOCK8R ? dst_scales != nullptr : !dst_scales) return CSA2_ERR_INVALID_ARG;
+    if (layout != CSA2_LAYOUT_ROWS && (dim != 128 || n_rows % 8)) return CSA2_ERR_UNSUPPORTED;
     int n_hi = 0;
     const float2* table = nullptr;
     if (pos != nullptr) {
@@ -322,13 +330,16 @@ extern "C" csa2_status csa2_quantize_append(const void* x_bf16, int64_t n, int d
     }
     timer_begin(K_QUANT_FP4, s);
     if (dim == 512)
-        launch(quantize_fp4_kernel<512, false>, grid_for(n, 8, kFp4BlocksPerSm), 256, 0, s, 1,
+        launch(quantize_fp4_kernel<512, CSA2_LAYOUT_ROWS>, grid_for(n, 8, kFp4BlocksPerSm), 256, 0, s, 1,
+            x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
+    else if (layout == CSA2_LAYOUT_BLOCK8R)
+        launch(quantize_fp4_kernel<128, CSA2_LAYOUT_BLOCK8R>, grid_for(n, 32, kFp4BlocksPerSm), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     else if (layout == CSA2_LAYOUT_BLOCK8)
-        launch(quantize_fp4_kernel<128, true>, grid_for(n, 32, kFp4BlocksPerSm), 256, 0, s, 1,
+        launch(quantize_fp4_kernel<128, CSA2_LAYOUT_BLOCK8>, grid_for(n, 32, kFp4BlocksPerSm), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     else
-        launch(quantize_fp4_kernel<128, false>, grid_for(n, 32, kFp4BlocksPerSm), 256, 0, s, 1,
+        launch(quantize_fp4_kernel<128, CSA2_LAYOUT_ROWS>, grid_for(n, 32, kFp4BlocksPerSm), 256, 0, s, 1,
             x, n, pos, table, n_hi, rope_max_pos, dst_row, n_rows, dst_codes, dst_scales, st);
     timer_end(K_QUANT_FP4, s);
     return launch_status();

@@ -75,9 +75,19 @@ constexpr int kTcSfLead = 3;         // tiles whose scales are staged ahead (< k
 constexpr int kTcMaxCandPerCta = 4096;
 static_assert(kTcMaxCandPerCta >= kMaxPoolBlocks, "a CTA stages at most all candidate blocks");
 
+// Indexer K arrives either as BLOCK8 code blocks of 512 bytes with the
+// scales in their own row-major plane, or as 576-byte records (a block's 512
+// code bytes, then its 8 rows x 8 scale bytes).  A stage holds one tile in
+// the same form: 16 x 512 code bytes then 16 x 64 scale bytes, or 16
+// records; the MMA reads the codes in place (8-row groups 512 or 576 bytes
+// apart).
+constexpr int kStageBytes = kTile * 72;
+__device__ __forceinline__ uint32_t stage_scale_off(bool rec, int row) {
+    return rec ? uint32_t((row >> 3) * 576 + 512 + (row & 7) * 8) : uint32_t(kTile * 64 + row * 8);
+}
+
 struct TcScanSmem {
-    uint8_t codes[kTcStages][kTile * 64];
-    uint8_t scales[kTcStages][kTile * 8];
+    uint8_t stage[kTcStages][kStageBytes];
     uint8_t qcodes[32 * 64];          // the query's 32 heads, BLOCK8 = canonical K-major
     int32_t cand[kTcMaxCandPerCta];   // this CTA's candidate blocks (pool scoring)
     uint64_t full[kTcStages], empty[kTcStages];
@@ -187,6 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride) {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
+    const bool rec = k_scales == nullptr;  // indexer K as 576-byte records
     grid_dep_wait();
     grid_dep_launch();
     int64_t q = blockIdx.y, t0, t1;
@@ -273,24 +284,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                     const int64_t nvb64 = nblk_vis - t * 16;
                     const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
                     mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
-                    bulk_g2s(S.codes[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
-                    bulk_g2s(S.scales[s], k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
+                    if (rec) {
+                        bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 576, nvb * 576, &S.full[s]);
+                    } else {
+                        bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
+                        bulk_g2s(S.stage[s] + kTile * 64, k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
+                    }
                 }
             } else {
-                const int j = lane & 15;  // block j of the tile: lane j its codes, lane 16 + j its scales
+                // block j of the tile: lane j its record (or its codes, and
+                // lane 16 + j its scales)
+                const int j = lane & 15;
                 const int64_t ci = t * 16 + j;
                 const int32_t bl = ci < C ? S.cand[ci - t0 * 16] : -1;
-                const bool live = bl >= 0 && bl < nblk_vis;
+                const bool live = bl >= 0 && bl < nblk_vis && (lane < 16 || !rec);
                 if (lane < 16 && !live && check_cand && (bl < -1 || bl >= nblk_vis))
                     record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), bl);
-                const uint32_t bytes = __reduce_add_sync(0xffffffffu, live ? (lane < 16 ? 512u : 64u) : 0u);
+                const uint32_t bytes = __reduce_add_sync(0xffffffffu, live ? (lane < 16 ? (rec ? 576u : 512u) : 64u) : 0u);
                 if (lane == 0) mbar_arrive_expect_tx(&S.full[s], bytes);  // 0 bytes: the phase completes at once
                 __syncwarp();
                 if (live) {
-                    if (lane < 16)
-                        bulk_g2s(S.codes[s] + j * 512, k_codes + ((ks >> 3) + bl) * 512, 512, &S.full[s]);
+                    if (rec)
+                        bulk_g2s(S.stage[s] + j * 576, k_codes + ((ks >> 3) + bl) * 576, 576, &S.full[s]);
+                    else if (lane < 16)
+                        bulk_g2s(S.stage[s] + j * 512, k_codes + ((ks >> 3) + bl) * 512, 512, &S.full[s]);
                     else
-                        bulk_g2s(S.scales[s] + j * 64, k_scales + (ks + 8 * int64_t(bl)) * 8, 64, &S.full[s]);
+                        bulk_g2s(S.stage[s] + kTile * 64 + j * 64, k_scales + (ks + 8 * int64_t(bl)) * 8, 64,
+                                 &S.full[s]);
                 }
             }
         }
@@ -305,11 +325,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                      (i < kTcAcc || mbar_wait(&S.acc_empty[a], ((i / kTcAcc) - 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t ka = smem_u32(S.codes[s]);
+                const uint32_t ka = smem_u32(S.stage[s]), sbo = rec ? 576 : 512;
                 const uint32_t d = tmem + kColAcc + 32 * a;
                 const uint32_t sfa = tmem + kColSfa + 8 * f, sfb = tmem + kColSfb;
-                mma_mxf4_ss(d, umma_desc(ka, 128, 512), umma_desc(qa, 128, 512), id, sfa, sfb, false);
-                mma_mxf4_ss(d, umma_desc(ka + 256, 128, 512), umma_desc(qa + 256, 128, 512), id, sfa + 4, sfb + 4, true);
+                mma_mxf4_ss(d, umma_desc(ka, 128, sbo), umma_desc(qa, 128, 512), id, sfa, sfb, false);
+                mma_mxf4_ss(d, umma_desc(ka + 256, 128, sbo), umma_desc(qa + 256, 128, 512), id, sfa + 4, sfb + 4, true);
                 tc_commit(&S.acc_full[a]);
                 tc_commit(&S.empty[s]);
             }
@@ -335,7 +355,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
             if (!mbar_wait(&S.full[s], (i / kTcStages) & 1)) return false;
             uint2 r4[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) r4[j] = *reinterpret_cast<const uint2*>(S.scales[s] + (lane + 32 * j) * 8);
+            for (int j = 0; j < 4; ++j)
+                r4[j] = *reinterpret_cast<const uint2*>(S.stage[s] + stage_scale_off(rec, lane + 32 * j));
             tmem_st4(lane_base + kColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
             tmem_st4(lane_base + kColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
             tmem_st_wait();
@@ -1240,8 +1261,7 @@ constexpr uint32_t kMqCols = 512;
 constexpr uint32_t kMqColSfa = 256, kMqColSfb = 288;  // scale slots (4 x 8 columns), query scales (8)
 
 struct MqSmem {
-    uint8_t codes[kTcStages][kTile * 64];
-    uint8_t scales[kTcStages][kTile * 8];
+    uint8_t stage[kTcStages][kStageBytes];
     uint8_t qcodes[kMqQ * 32 * 64];  // the run's query heads, BLOCK8 = canonical K-major
     float w[kMqQ * 32];
     int32_t n[kMqQ];
@@ -1260,6 +1280,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     float* __restrict__ out, int64_t out_stride, Status* st) {
     extern __shared__ __align__(1024) uint8_t mq_smem_raw[];
     MqSmem& S = *reinterpret_cast<MqSmem*>(mq_smem_raw);
+    const bool rec = k_scales == nullptr;  // indexer K as 576-byte records
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
     const int64_t q0 = int64_t(blockIdx.y) * kMqQ;
     const int nqg = int(n_q - q0 < kMqQ ? n_q - q0 : kMqQ);
@@ -1328,8 +1349,13 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                         const int64_t nvb64 = nblk - t * 16;
                         const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
                         mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
-                        bulk_g2s(S.codes[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
-                        bulk_g2s(S.scales[s], k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
+                        if (rec) {
+                            bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 576, nvb * 576, &S.full[s]);
+                        } else {
+                            bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
+                            bulk_g2s(S.stage[s] + kTile * 64, k_scales + (ks + t * kTile) * 8, nvb * 64,
+                                     &S.full[s]);
+                        }
                     }
                 }
             } else if (warp == 1) {  // --------------------------- MMA issue
@@ -1344,11 +1370,11 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                              (g < kMqAcc || mbar_wait(&S.acc_empty[a], ((g / kMqAcc) - 1) & 1));
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t ka = smem_u32(S.codes[s]);
+                        const uint32_t ka = smem_u32(S.stage[s]), sbo = rec ? 576 : 512;
                         const uint32_t d = tmem + 128 * a;
                         const uint32_t sfa = tmem + kMqColSfa + 8 * f, sfb = tmem + kMqColSfb;
-                        mma_mxf4_ss(d, umma_desc(ka, 128, 512), umma_desc(qa, 128, 512), id, sfa, sfb, false);
-                        mma_mxf4_ss(d, umma_desc(ka + 256, 128, 512), umma_desc(qa + 256, 128, 512), id, sfa + 4,
+                        mma_mxf4_ss(d, umma_desc(ka, 128, sbo), umma_desc(qa, 128, 512), id, sfa, sfb, false);
+                        mma_mxf4_ss(d, umma_desc(ka + 256, 128, sbo), umma_desc(qa + 256, 128, 512), id, sfa + 4,
                                     sfb + 4, true);
                         tc_commit(&S.acc_full[a]);
                         tc_commit(&S.empty[s]);
@@ -1382,7 +1408,8 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                     if (!mbar_wait(&S.full[s], (g / kTcStages) & 1)) return false;
                     uint2 r4[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) r4[j] = *reinterpret_cast<const uint2*>(S.scales[s] + (lane + 32 * j) * 8);
+                    for (int j = 0; j < 4; ++j)
+                        r4[j] = *reinterpret_cast<const uint2*>(S.stage[s] + stage_scale_off(rec, lane + 32 * j));
                     tmem_st4(lane_base + kMqColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
                     tmem_st4(lane_base + kMqColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
                     tmem_st_wait();
@@ -1451,9 +1478,9 @@ static csa2_status check_index_args(const uint8_t* q_codes, const uint8_t* q_sca
                                     const int32_t* n_visible, int32_t max_visible,
                                     int pool_blocks, int topk) {
     if (n_q < 0 || n_rows < 0 || max_visible < 0) return CSA2_ERR_INVALID_ARG;
-    if (!q_codes || !q_scales || !w || !k_codes || !k_scales || !kv_start || !n_visible)
-        return CSA2_ERR_INVALID_ARG;
-    if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(k_scales) || !aligned16(q_scales))
+    // k_scales NULL: k_codes holds 576-byte records (CSA2_LAYOUT_BLOCK8R)
+    if (!q_codes || !q_scales || !w || !k_codes || !kv_start || !n_visible) return CSA2_ERR_INVALID_ARG;
+    if (!aligned16(q_codes) || !aligned16(k_codes) || (k_scales && !aligned16(k_scales)) || !aligned16(q_scales))
         return CSA2_ERR_INVALID_ARG;
     if (n_rows % 8) return CSA2_ERR_UNSUPPORTED;
     if (pool_blocks < 1 || pool_blocks > kMaxPoolBlocks || topk < 1 || topk > kMaxTopk)

@@ -61,7 +61,7 @@ class LayerGroup:
     """Caches, per-layer inputs/outputs and workspaces of one workload."""
 
     def __init__(self, wl: W.Workload, device="cuda", sm_scale=1.0 / math.sqrt(512.0),
-                 rope_theta=10000.0, out_dtype=torch.float32):
+                 rope_theta=10000.0, out_dtype=torch.float32, ik_layout=abi.LAYOUT_BLOCK8R):
         self.wl = wl
         self.dev = torch.device(device)
         self.B = wl.batch
@@ -86,8 +86,15 @@ class LayerGroup:
         u8 = torch.uint8
         self.kv_codes = torch.zeros((self.n_rows, 256), dtype=u8, device=d)
         self.kv_scales = torch.zeros((self.n_rows, 32), dtype=u8, device=d)
-        self.ik_codes = torch.zeros((self.n_rows * 64,), dtype=u8, device=d)
-        self.ik_scales = torch.zeros((self.n_rows, 8), dtype=u8, device=d)
+        # indexer K: 576-byte records of 8 rows (codes then scales), or BLOCK8
+        # codes with a separate scale plane
+        self.ik_layout = ik_layout
+        if ik_layout == abi.LAYOUT_BLOCK8R:
+            self.ik_codes = torch.zeros((self.n_rows // 8 * 576,), dtype=u8, device=d)
+            self.ik_scales = None
+        else:
+            self.ik_codes = torch.zeros((self.n_rows * 64,), dtype=u8, device=d)
+            self.ik_scales = torch.zeros((self.n_rows, 8), dtype=u8, device=d)
         max_pos = int(max(self.n_rows, self.contexts.max() * wl.m + wl.m))
         self.rope_max_pos = max_pos
         self.rope = torch.empty(abi.csa2_rope_table_bytes(512, max_pos), dtype=u8, device=d)
@@ -158,7 +165,7 @@ class LayerGroup:
             rows = W.cache_rows(wl, r)
             k = torch.from_numpy(W.indexer_k(wl, r)).to(torch.bfloat16).to(d)
             dst = torch.arange(base, base + rows, dtype=torch.int64, device=d)
-            abi.csa2_quantize_append(k, rows, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0, dst,
+            abi.csa2_quantize_append(k, rows, 128, abi.FMT_FP4, self.ik_layout, None, None, 0, dst,
                                      self.n_rows, self.ik_codes, self.ik_scales, self.ws_app,
                                      self.ws_app.numel(), s)
             del k
@@ -201,7 +208,7 @@ class LayerGroup:
     # ------------------------------------------------------------ the step
     def append_token(self, s):
         """Append the current token (position n-1) of every request."""
-        abi.csa2_quantize_append(self.tok_ik, self.B, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None, 0,
+        abi.csa2_quantize_append(self.tok_ik, self.B, 128, abi.FMT_FP4, self.ik_layout, None, None, 0,
                                  self.tok_row, self.n_rows, self.ik_codes, self.ik_scales, self.ws_app,
                                  self.ws_app.numel(), s)
         abi.csa2_quantize_append(self.tok_latent, self.B, 512, abi.FMT_FP4, abi.LAYOUT_ROWS, self.tok_pos,

@@ -77,8 +77,14 @@ enum { CSA2_FMT_FP4 = 0, CSA2_FMT_FP8 = 1 };
  *   b = 16c + j of the row (c = 0..3).  Scales stay row-major [row][8].  Used
  *   for indexer K and indexer Q: a block of 8 rows is 512 contiguous bytes
  *   holding four 8-row x 16-byte tiles, the shape tensor cores read.
+ * CSA2_LAYOUT_BLOCK8R (FP4, dim 128 only): BLOCK8 with each block's scales
+ *   beside its codes: block b of 8 rows is a 576-byte record at byte 576*b,
+ *   its 512 code bytes as in BLOCK8 followed by the 8 rows x 8 scale bytes
+ *   (row r's scale byte g at 576*(r/8) + 512 + (r%8)*8 + g).  dst_scales
+ *   must be NULL.  Used for indexer K: a block the index gathers is then one
+ *   contiguous read instead of two.
  */
-enum { CSA2_LAYOUT_ROWS = 0, CSA2_LAYOUT_BLOCK8 = 1 };
+enum { CSA2_LAYOUT_ROWS = 0, CSA2_LAYOUT_BLOCK8 = 1, CSA2_LAYOUT_BLOCK8R = 2 };
 
 /* Output element type of csa2_sparse_attn. */
 enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
@@ -132,7 +138,8 @@ csa2_status csa2_rope_table_init(float theta, int dim, int64_t max_pos, void* ta
  *              (saturating at 448), codes = nearest E2M1 of x/s, ties to the
  *              even code, saturating at 6, sign kept; s == 0 gives zero codes.
  *              CSA2_FMT_FP8: each element to E4M3 (nearest-even, saturating).
- *   layout     CSA2_LAYOUT_ROWS or CSA2_LAYOUT_BLOCK8 (FP4, dim 128).
+ *   layout     CSA2_LAYOUT_ROWS, or CSA2_LAYOUT_BLOCK8 / CSA2_LAYOUT_BLOCK8R
+ *              (FP4, dim 128).
  *   dim        512 or 128 (FP4 and FP8 rows; BLOCK8 needs 128).
  *   pos        [n] int64 RoPE positions, or NULL for no RoPE.  Needs
  *              rope_table from csa2_rope_table_init for the same dim, covering
@@ -141,7 +148,8 @@ csa2_status csa2_rope_table_init(float theta, int dim, int64_t max_pos, void* ta
  *   dst_row    [n] int64 destination rows, or NULL for rows 0..n-1.  A row
  *              outside [0, n_rows) is skipped and recorded.
  *   dst_codes  codes plane of n_rows rows (FP4), or the FP8 byte plane.
- *   dst_scales scales plane [n_rows][dim/16] (FP4), NULL for FP8.
+ *   dst_scales scales plane [n_rows][dim/16] (FP4), NULL for FP8 and for
+ *              CSA2_LAYOUT_BLOCK8R (the scales sit in the records).
  *   n_rows     rows in the destination planes (BLOCK8: a multiple of 8).
  *   ws         at least CSA2_STATUS_BYTES bytes (status word).
  */
@@ -166,7 +174,8 @@ csa2_status csa2_quantize_append(const void* x_bf16, int64_t n, int dim, int fmt
  *     which contain every top-k position.)
  *   q_codes/q_scales: indexer Q, BLOCK8 layout, n_q*32 rows of 128 channels
  *     (row t*32+h is head h of query t).  w: [n_q][32] fp32.
- *   k_codes/k_scales: indexer K plane, BLOCK8 layout, n_rows rows.
+ *   k_codes/k_scales: indexer K plane, n_rows rows: BLOCK8 codes and
+ *     row-major scales, or (k_scales NULL) BLOCK8R records in k_codes.
  *   kv_start [n_q] int64 (multiples of 8), n_visible [n_q] int32, device.
  *   max_visible: host upper bound of n_visible (sizes the launch).
  *   pool_blocks in [1, 4096], topk in [1, 2048].

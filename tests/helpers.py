@@ -34,6 +34,36 @@ def rows_to_block8(rows):
     return np.ascontiguousarray(rows.reshape(n // 8, 8, 4, 16).transpose(0, 2, 1, 3)).reshape(-1)
 
 
+def rows_to_records(code_rows, scale_rows):
+    """Row-major codes [n][64] and scales [n][8] (n a multiple of 8) ->
+    BLOCK8R records (576 bytes per 8 rows)."""
+    n = code_rows.shape[0]
+    blk = rows_to_block8(code_rows).reshape(n // 8, 512)
+    return np.ascontiguousarray(np.concatenate([blk, np.asarray(scale_rows, np.uint8).reshape(n // 8, 64)],
+                                               axis=1)).reshape(-1)
+
+
+def records_to_rows(plane, n_rows):
+    """BLOCK8R records (576 bytes per 8 rows: codes as BLOCK8, then the 8
+    rows' 8 scale bytes) -> (codes [n_rows][64], scales [n_rows][8])."""
+    a = np.asarray(plane, dtype=np.uint8).reshape(n_rows // 8, 576)
+    codes = block8_to_rows(a[:, :512].reshape(-1), n_rows)
+    return codes, a[:, 512:].reshape(n_rows, 8)
+
+
+def indexer_k_planes(g, r0, r1):
+    """Rows [r0, r1) (r0 a multiple of 8) of a LayerGroup's indexer K as
+    (codes [rows][64], scales [rows][8]), whichever layout it uses."""
+    from csa2_sparse_attention_gb300 import abi
+    r1_8 = (r1 + 7) // 8 * 8
+    if g.ik_layout == abi.LAYOUT_BLOCK8R:
+        codes, scales = records_to_rows(g.ik_codes[r0 // 8 * 576:r1_8 // 8 * 576].cpu().numpy(), r1_8 - r0)
+    else:
+        codes = block8_to_rows(g.ik_codes[r0 * 64:r1_8 * 64].cpu().numpy(), r1_8 - r0)
+        scales = g.ik_scales[r0:r1_8].cpu().numpy()
+    return codes[:r1 - r0], scales[:r1 - r0]
+
+
 def check_selection(gpu_ids, oracle_ids, score_of, kth, label="", strict=False):
     """Sets equal except members whose score is within TOPK_REL of kth.
     gpu_ids must be ascending then -1 padded.  strict: the sets must be
@@ -97,10 +127,10 @@ def bf16_to_f64(t):
     return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
 
 
-def run_group(wl):
+def run_group(wl, **kw):
     import torch
     from csa2_sparse_attention_gb300.layer_group import LayerGroup
-    g = LayerGroup(wl)
+    g = LayerGroup(wl, **kw)
     for ws in (g.ws_app, g.ws_full, g.ws_re, g.ws_attn):
         ws.zero_()
     g.fill()
@@ -118,9 +148,9 @@ def verify_query(g, wl, q, check_cache=True):
     kdq = O.dequantize_fp4(kc, ks)
     lc, ls = O.quantize_fp4(O.rope(inp["latent_real"], inp["positions"]))
     if check_cache:
-        gk = block8_to_rows(g.ik_codes.cpu().numpy(), g.n_rows)[base:base + n]
+        gk, gs = indexer_k_planes(g, base, base + n)
         assert np.array_equal(gk, O.pack_codes(kc)), "indexer K bytes"
-        assert np.array_equal(g.ik_scales[base:base + n].cpu().numpy(), ks), "indexer K scales"
+        assert np.array_equal(gs, ks), "indexer K scales"
         gl = g.kv_codes[base:base + n].cpu().numpy()
         assert np.array_equal(gl, O.pack_codes(lc)), "main latent bytes"
         assert np.array_equal(g.kv_scales[base:base + n].cpu().numpy(), ls), "main latent scales"
@@ -195,10 +225,9 @@ def verify_query_at_scale(g, wl, q, cache_sample=2048, seed=7):
     rows = W.cache_rows(wl, r)
     # indexer K: every row of the query's view
     kc, ks = O.quantize_fp4(W.indexer_k_rows(wl, r, 0, n))
-    nb = (n + 7) // 8
-    plane = g.ik_codes[base * 64:(base + nb * 8) * 64].cpu().numpy()
-    assert np.array_equal(block8_to_rows(plane, nb * 8)[:n], O.pack_codes(kc)), f"q{q} indexer K bytes"
-    assert np.array_equal(g.ik_scales[base:base + n].cpu().numpy(), ks), f"q{q} indexer K scales"
+    gk, gs = indexer_k_planes(g, base, base + n)
+    assert np.array_equal(gk, O.pack_codes(kc)), f"q{q} indexer K bytes"
+    assert np.array_equal(gs, ks), f"q{q} indexer K scales"
     kdq = O.dequantize_fp4(kc, ks)
     del kc
     # indices: Full against the global definitions, Reindex on the GPU's pool

@@ -69,6 +69,16 @@ def test_host_argument_errors_return_before_launch(abi):
     st = A.lib.csa2_quantize_append(fake, 4, 96, A.FMT_FP4, A.LAYOUT_ROWS, None, None, 0, None, 4,
                                     fake, fake, fake, 256, None)
     assert st == A.ERR_UNSUPPORTED
+    # 576-byte records: scales live in the records (dst_scales must be NULL), dim 128 only
+    st = A.lib.csa2_quantize_append(fake, 4, 128, A.FMT_FP4, A.LAYOUT_BLOCK8R, None, None, 0, None, 8,
+                                    fake, fake, fake, 256, None)
+    assert st == A.ERR_INVALID_ARG
+    st = A.lib.csa2_quantize_append(fake, 4, 512, A.FMT_FP4, A.LAYOUT_BLOCK8R, None, None, 0, None, 8,
+                                    fake, None, fake, 256, None)
+    assert st == A.ERR_UNSUPPORTED
+    st = A.lib.csa2_quantize_append(fake, 4, 128, A.FMT_FP4, A.LAYOUT_BLOCK8, None, None, 0, None, 8,
+                                    fake, None, fake, 256, None)
+    assert st == A.ERR_INVALID_ARG  # BLOCK8 needs its scale plane
     st = A.lib.csa2_index_full(fake, fake, fake, 1, fake, fake, 12, fake, fake, 100, 2048, 512,
                                fake, fake, fake, 1 << 30, None)
     assert st == A.ERR_UNSUPPORTED  # n_rows not a multiple of 8

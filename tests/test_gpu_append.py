@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from oracle import csa2_oracle as O
-from tests.helpers import block8_to_rows
+from tests.helpers import block8_to_rows, records_to_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -24,8 +24,9 @@ def run_fp4(A, x, dim=128, layout=0, pos=None, dst=None, n_rows=None, table_pos=
     n = x.shape[0]
     n_rows = n if n_rows is None else n_rows
     xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).cuda()
-    codes = torch.zeros(n_rows * dim // 2, dtype=torch.uint8, device="cuda")
-    scales = torch.zeros((n_rows, dim // 16), dtype=torch.uint8, device="cuda")
+    rec = layout == A.LAYOUT_BLOCK8R
+    codes = torch.zeros(n_rows // 8 * 576 if rec else n_rows * dim // 2, dtype=torch.uint8, device="cuda")
+    scales = None if rec else torch.zeros((n_rows, dim // 16), dtype=torch.uint8, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     table, max_pos, pos_t = None, 0, None
     if pos is not None:
@@ -39,6 +40,9 @@ def run_fp4(A, x, dim=128, layout=0, pos=None, dst=None, n_rows=None, table_pos=
     torch.cuda.synchronize()
     st = A.csa2_status_fetch(ws)
     c = codes.cpu().numpy()
+    if rec:
+        c, sc = records_to_rows(c, n_rows)
+        return c, sc, st
     c = block8_to_rows(c, n_rows) if layout == A.LAYOUT_BLOCK8 else c.reshape(n_rows, dim // 2)
     return c, scales.cpu().numpy(), st
 
@@ -99,13 +103,16 @@ def test_fp8_every_bf16(A):
     assert np.array_equal(out.cpu().numpy(), O.e4m3_encode(x.astype(np.float64)))
 
 
-def test_block8_layout_with_destination_rows(A):
+@pytest.mark.parametrize("records", [False, True])
+def test_block8_layout_with_destination_rows(A, records):
+    """BLOCK8 codes with a scale plane, and BLOCK8R 576-byte records."""
     rng = np.random.default_rng(5)
     n_rows = 1000
     x = rng.normal(size=(600, 128)).astype(np.float32)
     x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
     dst = rng.permutation(n_rows)[:600]
-    codes, scales, st = run_fp4(A, x, layout=A.LAYOUT_BLOCK8, dst=dst, n_rows=n_rows)
+    codes, scales, st = run_fp4(A, x, layout=A.LAYOUT_BLOCK8R if records else A.LAYOUT_BLOCK8, dst=dst,
+                                n_rows=n_rows)
     assert st[0] == 0
     rc, rs = O.quantize_fp4(x.astype(np.float64))
     assert np.array_equal(codes[dst], O.pack_codes(rc))

@@ -17,11 +17,14 @@ from tests.helpers import bf16_to_f64, check_attention, check_status, run_group,
 pytestmark = pytest.mark.gpu
 
 
-def test_tiny_group_8k():
+@pytest.mark.parametrize("records", [True, False])
+def test_tiny_group_8k(records):
     """8192 entries, Full + Reindex + Reuse, pool 256 x 8 (smaller than
-    top-512: the Full top-k comes from the top-512 blocks)."""
+    top-512: the Full top-k comes from the top-512 blocks); indexer K as
+    576-byte records or as BLOCK8 codes with a scale plane."""
+    from csa2_sparse_attention_gb300 import abi
     wl = W.tiny()
-    g = run_group(wl)
+    g = run_group(wl, ik_layout=abi.LAYOUT_BLOCK8R if records else abi.LAYOUT_BLOCK8)
     check_status(g)
     verify_query(g, wl, 0)
     # the Reuse layer attends over the Reindex layer's own top-k buffer (the

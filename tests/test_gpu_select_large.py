@@ -21,14 +21,15 @@ import pytest
 import torch
 
 from oracle import csa2_oracle as O
-from tests.helpers import check_selection, kth_value, rows_to_block8
+from tests.helpers import check_selection, kth_value, rows_to_block8, rows_to_records
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("contexts", [(300_000, 50_000, 262_143), (1_600_000, 1_000_003),
-                                      (65_536, 65_537, 131_072, 131_073, 8_000)])
-def test_pool_and_topk_at_selection_path_boundaries(contexts):
+@pytest.mark.parametrize("contexts,records", [((300_000, 50_000, 262_143), False), ((1_600_000, 1_000_003), True),
+                                              ((65_536, 65_537, 131_072, 131_073, 8_000), True)])
+def test_pool_and_topk_at_selection_path_boundaries(contexts, records):
+    """(Indexer K as BLOCK8 codes with a scale plane, or as 576-byte records.)"""
     from csa2_sparse_attention_gb300 import abi
     rng = np.random.default_rng(sum(contexts))
     n_q, P, K = len(contexts), 2048, 512
@@ -40,8 +41,12 @@ def test_pool_and_topk_at_selection_path_boundaries(contexts):
     kv_start = np.concatenate([[0], np.cumsum(rows_of)[:-1]]).astype(np.int64)
     n_rows = int(sum(rows_of))
     row_id = rng.integers(0, 16, n_rows)
-    k_codes = torch.from_numpy(rows_to_block8(pk16[row_id])).cuda()
-    k_scales = torch.from_numpy(np.ascontiguousarray(ks16[row_id])).cuda()
+    if records:
+        k_codes = torch.from_numpy(rows_to_records(pk16[row_id], ks16[row_id])).cuda()
+        k_scales = None
+    else:
+        k_codes = torch.from_numpy(rows_to_block8(pk16[row_id])).cuda()
+        k_scales = torch.from_numpy(np.ascontiguousarray(ks16[row_id])).cuda()
     q_real = torch.randn((n_q * 32, 128), generator=torch.Generator().manual_seed(22)).to(torch.bfloat16)
     qc, qs = O.quantize_fp4(q_real.float().numpy().astype(np.float64))
     q_codes = torch.from_numpy(rows_to_block8(O.pack_codes(qc))).cuda()
