@@ -47,6 +47,7 @@ EXPORTS = {
     "csa2_index_reindex_noalloc": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p,
                                           _p, _p]),
     "csa2_launch_count": (_i64, []),
+    "csa2_debug_wait_limit": (_int, [_i64]),
     "csa2_kernel_name": (ctypes.c_char_p, [_int]),
     "csa2_timer_enable": (_int, [_int, _int]),
     "csa2_timer_read": (_int, [_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i32)]),
@@ -164,6 +165,11 @@ KERNELS = ("scan_blockmax", "select_blocks", "pool_score", "select_topk", "attn_
 
 def csa2_launch_count():
     return lib.csa2_launch_count()
+
+
+def csa2_debug_wait_limit(ns):
+    """Test hook: the bounded device waits' limit in ns for later launches (0: 2 s)."""
+    return _check("csa2_debug_wait_limit", lib.csa2_debug_wait_limit(ns))
 
 
 def csa2_kernel_name(kernel_id):

@@ -12,6 +12,21 @@ csa2_status launch_status() {
     return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
+int sm_count() {
+    static std::atomic<int> cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 148;
+        }
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 // ---- instrumentation: launch counter and per-kernel event pairs
 static std::atomic<int64_t> g_launches{0};
 struct KernelTimer {
@@ -95,6 +110,15 @@ extern "C" csa2_status csa2_status_fetch(const void* ws, int32_t out[4], csa2_st
 }
 
 extern "C" int64_t csa2_launch_count(void) { return g_launches.load(); }
+
+extern "C" csa2_status csa2_debug_wait_limit(int64_t ns) {
+    if (ns < 0) return CSA2_ERR_INVALID_ARG;
+    if (set_wait_limit_index(uint64_t(ns)) != cudaSuccess || set_wait_limit_attn(uint64_t(ns)) != cudaSuccess) {
+        cudaGetLastError();
+        return CSA2_ERR_CUDA;
+    }
+    return CSA2_OK;
+}
 
 extern "C" const char* csa2_kernel_name(int kernel_id) {
     return (kernel_id >= 0 && kernel_id < K_COUNT) ? kKernelNames[kernel_id] : "unknown";

@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(
 // that are resident at once (per_sm per SM), which then stride the rows.
 static int grid_for(int64_t rows, int rows_per_block, int per_sm = 16) {
     int64_t g = ceil_div<int64_t>(rows, rows_per_block);
-    const int64_t cap = int64_t(kSMs) * per_sm;
+    const int64_t cap = int64_t(sm_count()) * per_sm;
     return int(g < 1 ? 1 : (g > cap ? cap : g));
 }
 constexpr int kFp4BlocksPerSm = 3;  // quantize_fp4_kernel's launch bound

@@ -616,6 +616,9 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     if (lse && lane == 0) lse[q * kH + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
+// The bounded waits' limit of this unit's kernels (a test hook).
+cudaError_t set_wait_limit_attn(uint64_t ns) { return set_wait_limit(ns); }
+
 // Opt both variants into their shared memory and note how many clusters of
 // `splits` CTAs can be resident at once (0 when clusters are unavailable).
 static csa2_status prepare_attn_tc(int splits, int* max_clusters) {

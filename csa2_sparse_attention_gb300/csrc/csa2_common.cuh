@@ -146,6 +146,9 @@ __host__ __device__ constexpr T ceil_div(T a, T b) { return (a + b - 1) / b; }
 namespace csa2 {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 csa2_status launch_status();  // maps cudaGetLastError to a csa2_status
+int sm_count();               // the current device's multiprocessors (queried once per device)
+cudaError_t set_wait_limit_index(uint64_t ns);  // the bounded waits' limit, per translation unit
+cudaError_t set_wait_limit_attn(uint64_t ns);
 
 // Launches `kernel` on `s` with programmatic stream serialization (see
 // grid_dep_wait) and, when cluster > 1, clusters of `cluster` CTAs along x.

@@ -98,8 +98,10 @@ struct TcScanSmem {
     int abort_flag;
 };
 
-constexpr int kScanMaxQ = kSMs;  // queries the balanced scan mapping handles (one wave of 2 x SMs)
-static_assert(2 * kSMs - kScanMaxQ >= kSMs, "one wave holds the CTAs of every active query");
+// Queries the balanced scan mapping handles (its per-lane register arrays);
+// it runs only when the batch also fits the device's SM count, so that one
+// wave of two CTAs per SM holds a CTA of every active query.
+constexpr int kScanMaxQ = 152;
 
 
 // The balanced scan mapping over a grid of G CTAs (b = this CTA's linear
@@ -261,6 +263,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = S.tmem;
+    // (warp 0 lane 0) tiles whose copies were issued; (warp 1 lane 0) tiles
+    // whose MMAs were issued: what a give-up must wait for before TMEM and
+    // shared memory are released
+    int issued = 0, mma_n = 0;
 
     if (warp == 0) {  // ------------------------------------------ producer
         // the scan copies a tile with two bulk copies from lane 0; the gather
@@ -271,8 +277,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         }
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % kTcStages, r = i / kTcStages;
-            int ok = 1;
-            if (lane == 0 && r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
+            int ok = *reinterpret_cast<volatile int*>(&S.abort_flag) == 0;
+            if (ok && lane == 0 && r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
                 record(st, CSA2_ERR_TIMEOUT, 10, int32_t(q), i);
                 S.abort_flag = 1;
                 ok = 0;
@@ -291,6 +297,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                         bulk_g2s(S.stage[s] + kTile * 64, k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
                     }
                 }
+                issued = i + 1;
             } else {
                 // block j of the tile: lane j its record (or its codes, and
                 // lane 16 + j its scales)
@@ -312,6 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                         bulk_g2s(S.stage[s] + kTile * 64 + j * 64, k_scales + (ks + 8 * int64_t(bl)) * 8, 64,
                                  &S.full[s]);
                 }
+                issued = i + 1;
             }
         }
     } else if (warp == 1) {  // ----------------------------------- MMA issue
@@ -332,6 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                 mma_mxf4_ss(d, umma_desc(ka + 256, 128, sbo), umma_desc(qa + 256, 128, 512), id, sfa + 4, sfb + 4, true);
                 tc_commit(&S.acc_full[a]);
                 tc_commit(&S.empty[s]);
+                mma_n = i + 1;
             }
             if (!ok) {
                 record(st, CSA2_ERR_TIMEOUT, 11, int32_t(q), 0);
@@ -367,6 +376,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         bool ok = true;
         for (int i = 0; ok && i < kTcSfLead && i < ntiles; ++i) ok = stage_sf(i);
         for (int i = 0; ok && i < ntiles; ++i) {
+            if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
+                ok = false;
+                break;
+            }
             // tile i + lead reuses the slot of tile i + lead - kTcSf, whose MMA
             // finished before tile i - 1's accumulator was read
             if (i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
@@ -406,6 +419,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         if (!ok && lane == 0) {
             record(st, CSA2_ERR_TIMEOUT, 12, int32_t(q), 0);
             S.abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (S.abort_flag && lane == 0) {
+        // a wait gave up: wait for the copies and MMAs already issued (the
+        // last commit covers every earlier MMA) before anything is released
+        if (warp == 0) {
+            mbar_wait(&S.qbar, 0, kDrainNs);
+            for (int i = issued > kTcStages ? issued - kTcStages : 0; i < issued; ++i)
+                mbar_wait(&S.full[i % kTcStages], (i / kTcStages) & 1, kDrainNs);
+        } else if (warp == 1 && mma_n > 0) {
+            mbar_wait(&S.empty[(mma_n - 1) % kTcStages], ((mma_n - 1) / kTcStages) & 1, kDrainNs);
         }
     }
     tc_fence_before();
@@ -1315,6 +1341,9 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     const int quad = warp & 3;
     const uint32_t lane_base = tmem + (uint32_t(32 * quad) << 16);
     int it = 0;   // tiles issued so far (ring, slot and accumulator phases)
+    // (warp 0 lane 0) tiles whose copies were issued and Q copies; (warp 1
+    // lane 0) tiles whose MMAs were issued: what a give-up must wait for
+    int issued = 0, q_copies = 0, mma_n = 0;
     int run = 0;  // runs so far (Q phase)
     for (int r0 = 0; r0 < nqg;) {
         int r1 = r0 + 1;  // [r0, r1): queries with the same row range start, and something visible
@@ -1338,6 +1367,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&S.qbar, uint32_t(nr) * 32 * 64);
                     bulk_g2s(S.qcodes, q_codes + ((q0 + r0) * 32 / 8) * 512, uint32_t(nr) * 32 * 64, &S.qbar);
+                    ++q_copies;
                     for (int i = 0; i < ntiles; ++i) {
                         const int g = it + i, s = g % kTcStages, rr = g / kTcStages;
                         if (rr > 0 && !mbar_wait(&S.empty[s], (rr - 1) & 1)) {
@@ -1356,6 +1386,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                             bulk_g2s(S.stage[s] + kTile * 64, k_scales + (ks + t * kTile) * 8, nvb * 64,
                                      &S.full[s]);
                         }
+                        issued = g + 1;
                     }
                 }
             } else if (warp == 1) {  // --------------------------- MMA issue
@@ -1378,6 +1409,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                                     sfb + 4, true);
                         tc_commit(&S.acc_full[a]);
                         tc_commit(&S.empty[s]);
+                        mma_n = g + 1;
                     }
                     if (!ok) {
                         record(st, CSA2_ERR_TIMEOUT, 21, int32_t(q0 + r0), 0);
@@ -1468,6 +1500,19 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     }
     tc_fence_before();
     __syncthreads();
+    if (S.abort_flag && lane == 0) {
+        // a wait gave up: wait for the copies and MMAs already issued (the
+        // last commit covers every earlier MMA) before anything is released
+        if (warp == 0) {
+            if (q_copies > 0) mbar_wait(&S.qbar, (q_copies - 1) & 1, kDrainNs);
+            for (int g = issued > kTcStages ? issued - kTcStages : 0; g < issued; ++g)
+                mbar_wait(&S.full[g % kTcStages], (g / kTcStages) & 1, kDrainNs);
+        } else if (warp == 1 && mma_n > 0) {
+            mbar_wait(&S.empty[(mma_n - 1) % kTcStages], ((mma_n - 1) / kTcStages) & 1, kDrainNs);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, kMqCols);
 }
 
@@ -1517,10 +1562,13 @@ static csa2_status prepare_select_kernels() {
     return CSA2_OK;
 }
 
+// The bounded waits' limit of this unit's kernels (a test hook).
+cudaError_t set_wait_limit_index(uint64_t ns) { return set_wait_limit(ns); }
+
 // CTAs per query for a tensor-core scorer launch: two resident CTAs per SM
 // over the whole batch, at most one per tile.
 static int64_t tc_ctas_per_query(int64_t n_q, int64_t tiles_max) {
-    int64_t cpq = 2 * kSMs / n_q;
+    int64_t cpq = 2 * int64_t(sm_count()) / n_q;
     return cpq < 1 ? 1 : (cpq > tiles_max ? tiles_max : cpq);
 }
 
@@ -1614,7 +1662,7 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         // many queries: groups of 4 share each K tile; about 8 waves of one CTA per SM
         const int64_t groups = ceil_div<int64_t>(n_q, kMqQ);
         const int64_t tiles = ceil_div<int64_t>(max_visible, kTile);
-        int64_t chunks = ceil_div<int64_t>(8 * kSMs, groups);
+        int64_t chunks = ceil_div<int64_t>(8 * int64_t(sm_count()), groups);
         chunks = chunks < 1 ? 1 : (chunks > tiles ? tiles : chunks);
         timer_begin(K_SCAN, s);
         launch(scan_mq_kernel, dim3(unsigned(chunks), unsigned(groups)), kMqThreads, sizeof(MqSmem), s, 1, q_codes,
@@ -1627,7 +1675,7 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         timer_begin(K_SCAN, s);
         launch(score_tc_kernel<false>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0,
-            n_q <= kScanMaxQ ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st,
+            (n_q <= kScanMaxQ && n_q <= sm_count()) ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st,
             L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride);
         timer_end(K_SCAN, s);
     }

@@ -9,7 +9,6 @@
 namespace csa2 {
 
 constexpr int kMaxWindow = 128;
-constexpr int kSMs = 152;            // GB300 streaming multiprocessors
 constexpr int kMaxPoolBlocks = 4096;
 constexpr int kMaxTopk = 2048;
 

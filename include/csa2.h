@@ -279,6 +279,18 @@ csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q,
  *   the number of launches timed, and switch the timer off.
  */
 int64_t csa2_launch_count(void);
+
+/*
+ * Test hook for the device give-up paths.  Every wait of a library kernel on
+ * a barrier (copies arriving, MMAs completing) is bounded: after 2 s it
+ * records CSA2_ERR_TIMEOUT in the status word, stops issuing work, waits for
+ * the copies and MMAs it already started, and returns.  csa2_debug_wait_limit
+ * sets that limit (in nanoseconds) for kernels launched afterwards on the
+ * current device; 0 restores 2 s.  A short limit makes the waits give up on
+ * purpose, so a test can check the status and that the next normal call is
+ * correct.  Not for production use and not during stream capture.
+ */
+csa2_status csa2_debug_wait_limit(int64_t ns);
 const char* csa2_kernel_name(int kernel_id);
 csa2_status csa2_timer_enable(int kernel_id, int max_launches);
 csa2_status csa2_timer_read(int kernel_id, double* total_ms, int32_t* launches);

@@ -69,6 +69,7 @@ def test_host_argument_errors_return_before_launch(abi):
     st = A.lib.csa2_quantize_append(fake, 4, 96, A.FMT_FP4, A.LAYOUT_ROWS, None, None, 0, None, 4,
                                     fake, fake, fake, 256, None)
     assert st == A.ERR_UNSUPPORTED
+    assert A.lib.csa2_debug_wait_limit(-1) == A.ERR_INVALID_ARG  # checked before any device call
     # 576-byte records: scales live in the records (dst_scales must be NULL), dim 128 only
     st = A.lib.csa2_quantize_append(fake, 4, 128, A.FMT_FP4, A.LAYOUT_BLOCK8R, None, None, 0, None, 8,
                                     fake, fake, fake, 256, None)
