@@ -9,7 +9,7 @@ decoder group at 131,072 entries with batch 16 ([Full + 3 Reuse] +
 4 x [Reindex + 3 Reuse]).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 128k|1m|tiny|manyq|ragged]
+                    [--workload 128k|1m|tiny|manyq|ragged|encoder|append]
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
 (independent requests, no collective on the data path); value = all queries
@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def workload(name):
     from csa2_sparse_attention_gb300 import workloads as W
     return {"128k": W.group_128k, "1m": W.group_1m, "tiny": W.tiny, "manyq": W.many_query,
-            "ragged": W.ragged}[name]()
+            "ragged": W.ragged, "encoder": W.encoder_m2}[name]()
 
 
 def peaks():
@@ -670,7 +670,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="128k", choices=["128k", "1m", "tiny", "manyq", "ragged", "append"])
+    ap.add_argument("--workload", default="128k",
+                    choices=["128k", "1m", "tiny", "manyq", "ragged", "encoder", "append"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-second", action="store_true", help="skip the 1M group the default 128K line also reports")

@@ -44,6 +44,8 @@ EXPORTS = {
     "csa2_index_reindex": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p, _p, _sz, _p]),
     "csa2_sparse_attn": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _p, _int, ctypes.c_float,
                                 _p, _int, _p, _p, _sz, _p]),
+    "csa2_sparse_attn_prefill": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _int, ctypes.c_float,
+                                        _p, _int, _p, _p, _sz, _p]),
     "csa2_index_reindex_noalloc": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p,
                                           _p, _p]),
     "csa2_launch_count": (_i64, []),
@@ -157,6 +159,14 @@ def csa2_sparse_attn(q_bf16, n_q, kv_codes, kv_scales, n_rows, kv_start, n_visib
         _ptr(q_bf16), n_q, _ptr(kv_codes), _ptr(kv_scales), n_rows, _ptr(kv_start), _ptr(n_visible),
         _ptr(topk), k, _ptr(swa), _ptr(swa_new_bf16), window, sm_scale, _ptr(out), out_dtype,
         _ptr(out_lse), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def csa2_sparse_attn_prefill(q_bf16, n_q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa_rows,
+                             window, sm_scale, out, out_dtype, out_lse, ws, ws_bytes, stream=None):
+    return _check("csa2_sparse_attn_prefill", lib.csa2_sparse_attn_prefill(
+        _ptr(q_bf16), n_q, _ptr(kv_codes), _ptr(kv_scales), n_rows, _ptr(kv_start), _ptr(n_visible),
+        _ptr(topk), k, _ptr(swa_rows), window, sm_scale, _ptr(out), out_dtype, _ptr(out_lse), _ptr(ws),
+        ws_bytes, _stream(stream)))
 
 
 KERNELS = ("scan_blockmax", "select_blocks", "pool_score", "select_topk", "attn_split",

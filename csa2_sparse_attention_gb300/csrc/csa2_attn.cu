@@ -143,12 +143,15 @@ __device__ __forceinline__ void fp8_quarter_to_c(const uint4* v, uint8_t* c, int
 // grid (splits, n_q), 256 threads, one CTA per SM.  The split's unnormalized
 // partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [64][512]) and (m_s, l_s) per
 // head go to the workspace, or (CLUSTER) are merged across the cluster.
+// win_shared: the window rows come from swa [n_rows][512] at row kv_start +
+// position (a window over a sequence the queries share) instead of each
+// query's ring swa [n_q][window][512] at slot position mod window.
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const uint16_t* __restrict__ qg, const uint8_t* __restrict__ kv_codes,
     const uint8_t* __restrict__ kv_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, const int32_t* __restrict__ topk, int k,
-    uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, float sm_scale,
+    uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, bool win_shared, float sm_scale,
     float* __restrict__ part_o, float* __restrict__ part_ml, int splits, void* __restrict__ out,
     bool out_f32, float* __restrict__ out_lse, Status* st) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -238,7 +241,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         } else {
             kind = 2;
             const int64_t pos = int64_t(n - nw) + (ge - k);
-            const uint4* ring = reinterpret_cast<const uint4*>(swa + (q * window + pos % window) * kD);
+            const uint4* ring = reinterpret_cast<const uint4*>(
+                swa + (win_shared ? ks + pos : q * window + pos % window) * kD);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 rv[j] = ring[qa * 8 + j];
@@ -661,13 +665,13 @@ static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
 
 using namespace csa2;
 
-extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* kv_codes,
-                                        const uint8_t* kv_scales, int64_t n_rows,
-                                        const int64_t* kv_start, const int32_t* n_visible,
-                                        const int32_t* topk, int k, uint8_t* swa,
-                                        const void* swa_new_bf16, int window, float sm_scale, void* out,
-                                        int out_dtype, float* out_lse, void* ws, size_t ws_bytes,
-                                        csa2_stream_t stream) {
+// csa2_sparse_attn and csa2_sparse_attn_prefill: swa is a ring per query
+// (win_shared false) or rows of the shared sequence (true).
+static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* kv_codes, const uint8_t* kv_scales,
+                               int64_t n_rows, const int64_t* kv_start, const int32_t* n_visible,
+                               const int32_t* topk, int k, uint8_t* swa, const void* swa_new_bf16, int window,
+                               bool win_shared, float sm_scale, void* out, int out_dtype, float* out_lse, void* ws,
+                               size_t ws_bytes, cudaStream_t s) {
     if (n_q < 0 || n_rows < 0 || k < 0 || k > kMaxTopk || window < 0 || window > kMaxWindow)
         return CSA2_ERR_INVALID_ARG;
     if (!(sm_scale > 0.f) || !(sm_scale < FLT_MAX)) return CSA2_ERR_INVALID_ARG;
@@ -675,7 +679,7 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     if (!q_bf16 || !kv_codes || !kv_scales || !kv_start || !n_visible || !out) return CSA2_ERR_INVALID_ARG;
     if (k > 0 && !topk) return CSA2_ERR_INVALID_ARG;
     if (window > 0 && !swa) return CSA2_ERR_INVALID_ARG;
-    if (swa_new_bf16 && (window == 0 || !aligned16(swa_new_bf16))) return CSA2_ERR_INVALID_ARG;
+    if (swa_new_bf16 && (window == 0 || win_shared || !aligned16(swa_new_bf16))) return CSA2_ERR_INVALID_ARG;
     if (!aligned16(q_bf16) || !aligned16(kv_codes) || !aligned16(out) || (swa && !aligned16(swa)))
         return CSA2_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(kv_scales) & 7) return CSA2_ERR_INVALID_ARG;
@@ -683,7 +687,6 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     const AttnWs L = attn_ws(n_q, k, window);
     if (!ws || !aligned16(ws) || ws_bytes < L.total) return CSA2_ERR_WORKSPACE;
     if (n_q == 0) return CSA2_OK;
-    cudaStream_t s = cudaStream_t(stream);
     char* base = static_cast<char*>(ws);
     Status* st = reinterpret_cast<Status*>(base);
     float* part_o = reinterpret_cast<float*>(base + L.part_o);
@@ -700,11 +703,11 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
     timer_begin(K_ATTN_SPLIT, s);
     const cudaError_t le =
         cluster ? launch(attn_tc_kernel<true>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
-                         kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, sm_scale, part_o,
-                         part_ml, L.splits, out, f32, out_lse, st)
+                         kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
+                         sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st)
                 : launch(attn_tc_kernel<false>, grid, kAttnThreads, sizeof(AttnTcSmem), s, 1, q, kv_codes,
-                         kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, sm_scale, part_o, part_ml,
-                         L.splits, out, f32, out_lse, st);
+                         kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared, sm_scale,
+                         part_o, part_ml, L.splits, out, f32, out_lse, st);
     timer_end(K_ATTN_SPLIT, s);
     if (le != cudaSuccess) return CSA2_ERR_CUDA;
     if (cluster) return launch_status();
@@ -717,4 +720,26 @@ extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const u
                out_lse);
     timer_end(K_ATTN_MERGE, s);
     return launch_status();
+}
+
+extern "C" csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* kv_codes,
+                                        const uint8_t* kv_scales, int64_t n_rows,
+                                        const int64_t* kv_start, const int32_t* n_visible,
+                                        const int32_t* topk, int k, uint8_t* swa,
+                                        const void* swa_new_bf16, int window, float sm_scale, void* out,
+                                        int out_dtype, float* out_lse, void* ws, size_t ws_bytes,
+                                        csa2_stream_t stream) {
+    return sparse_attn(q_bf16, n_q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, swa_new_bf16,
+                       window, false, sm_scale, out, out_dtype, out_lse, ws, ws_bytes, cudaStream_t(stream));
+}
+
+extern "C" csa2_status csa2_sparse_attn_prefill(const void* q_bf16, int64_t n_q, const uint8_t* kv_codes,
+                                                const uint8_t* kv_scales, int64_t n_rows,
+                                                const int64_t* kv_start, const int32_t* n_visible,
+                                                const int32_t* topk, int k, const uint8_t* swa_rows, int window,
+                                                float sm_scale, void* out, int out_dtype, float* out_lse,
+                                                void* ws, size_t ws_bytes, csa2_stream_t stream) {
+    return sparse_attn(q_bf16, n_q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k,
+                       const_cast<uint8_t*>(swa_rows), nullptr, window, true, sm_scale, out, out_dtype, out_lse, ws,
+                       ws_bytes, cudaStream_t(stream));
 }

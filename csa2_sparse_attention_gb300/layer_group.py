@@ -100,7 +100,12 @@ class LayerGroup:
         self.rope = torch.empty(abi.csa2_rope_table_bytes(512, max_pos), dtype=u8, device=d)
         abi.csa2_rope_table_init(rope_theta, 512, max_pos, self.rope, torch.cuda.current_stream(d))
         L = len(self.layers)
-        self.swa = [torch.zeros((self.B, self.Wn, 512), dtype=u8, device=d) for _ in range(L)]
+        # window latents per layer: a ring per query (decode), or one E4M3 row
+        # per position of the shared sequence (prefill over a shared cache)
+        if wl.shared_window:
+            self.swa = [torch.zeros((self.n_rows, 512), dtype=u8, device=d) for _ in range(L)]
+        else:
+            self.swa = [torch.zeros((self.B, self.Wn, 512), dtype=u8, device=d) for _ in range(L)]
         self.out_dtype = out_dtype
         self.out_code = abi.OUT_F32 if out_dtype == torch.float32 else abi.OUT_BF16
         self.index_layers = [i for i, m in enumerate(self.layers) if m in (W.FULL, W.REINDEX)]
@@ -135,7 +140,11 @@ class LayerGroup:
         self.iq_scales = {i: torch.zeros((self.B * 32, 8), dtype=u8, device=d) for i in self.index_layers}
         self.iw = {i: vin[vid[i, "iw"]] for i in self.index_layers}
         self.topk = {i: torch.full((self.B, self.K), -1, dtype=torch.int32, device=d) for i in self.index_layers}
-        self.pool = torch.full((self.B, self.P), -1, dtype=torch.int32, device=d)
+        # one pool per Full layer (its group's Reindex layers read it); .pool
+        # is the first group's
+        self.full_layers = [i for i, m in enumerate(self.layers) if m == W.FULL]
+        self.pools = {i: torch.full((self.B, self.P), -1, dtype=torch.int32, device=d) for i in self.full_layers}
+        self.pool = self.pools[self.full_layers[0]]
         # per layer, the top-k tensor its attention call was given (Reuse
         # layers get their index source's buffer itself, not a copy)
         self.attn_index = {}
@@ -183,14 +192,25 @@ class LayerGroup:
         s = stream or torch.cuda.current_stream(d)
         bf = torch.bfloat16
         for li in range(len(self.layers)):
-            rings = np.stack([W.swa_ring(wl, q, li) for q in range(self.B)])
-            ring_t = torch.from_numpy(rings.reshape(-1, 512)).to(bf).to(d)
-            abi.csa2_quantize_append(ring_t, ring_t.shape[0], 512, abi.FMT_FP8, abi.LAYOUT_ROWS, None, None, 0,
-                                     None, self.B * self.Wn, self.swa[li], None, self.ws_app,
-                                     self.ws_app.numel(), s)
+            if wl.shared_window:  # the layer's window latents over the whole shared sequence
+                step = 65536
+                for r0 in range(0, wl.cache_entries, step):
+                    r1 = min(wl.cache_entries, r0 + step)
+                    rows_t = torch.from_numpy(W.swa_seq_rows(wl, li, r0, r1)).to(bf).to(d)
+                    dst = torch.arange(r0, r1, dtype=torch.int64, device=d)
+                    abi.csa2_quantize_append(rows_t, r1 - r0, 512, abi.FMT_FP8, abi.LAYOUT_ROWS, None, None, 0,
+                                             dst, self.n_rows, self.swa[li], None, self.ws_app,
+                                             self.ws_app.numel(), s)
+                    s.synchronize()
+            else:
+                rings = np.stack([W.swa_ring(wl, q, li) for q in range(self.B)])
+                ring_t = torch.from_numpy(rings.reshape(-1, 512)).to(bf).to(d)
+                abi.csa2_quantize_append(ring_t, ring_t.shape[0], 512, abi.FMT_FP8, abi.LAYOUT_ROWS, None, None,
+                                         0, None, self.B * self.Wn, self.swa[li], None, self.ws_app,
+                                         self.ws_app.numel(), s)
+                last = self.contexts - 1
+                self.tok_swa[li].copy_(torch.from_numpy(rings[np.arange(self.B), last % self.Wn]).to(bf))
             self.attn_q[li].copy_(torch.from_numpy(np.stack([W.attn_q(wl, q, li) for q in range(self.B)])).to(bf))
-            last = self.contexts - 1
-            self.tok_swa[li].copy_(torch.from_numpy(rings[np.arange(self.B), last % self.Wn]).to(bf))
             if li in self.index_layers:
                 self.iq_bf16[li].copy_(torch.from_numpy(
                     np.stack([W.indexer_q(wl, q, li) for q in range(self.B)]).reshape(-1, 128)).to(bf))
@@ -232,18 +252,28 @@ class LayerGroup:
         if mode == W.FULL:
             abi.csa2_index_full(self.iq_codes[li], self.iq_scales[li], self.iw[li], B, self.ik_codes,
                                 self.ik_scales, self.n_rows, self.kv_start, self.n_visible, self.max_visible,
-                                self.P, self.K, self.pool, self.topk[li], self.ws_full, self.ws_full.numel(), s)
+                                self.P, self.K, self.pools[li], self.topk[li], self.ws_full, self.ws_full.numel(), s)
         elif mode == W.REINDEX:
             abi.csa2_index_reindex(self.iq_codes[li], self.iq_scales[li], self.iw[li], B, self.ik_codes,
                                    self.ik_scales, self.n_rows, self.kv_start, self.n_visible,
-                                   self.max_visible, self.pool, self.P, self.K, self.topk[li], self.ws_re,
-                                   self.ws_re.numel(), s)
+                                   self.max_visible, self.pools[self.group_full(li)], self.P, self.K,
+                                   self.topk[li], self.ws_re, self.ws_re.numel(), s)
+
+    def group_full(self, li):
+        """The Full layer whose pool layer li's group uses."""
+        return max(i for i in self.full_layers if i <= li)
 
     def layer_attn(self, li, s, swa_append=True):
         """The attention of a layer over its index source's top-k."""
         B = self.B
         idx = self.topk[W.index_source(self.wl, li)]
         self.attn_index[li] = idx
+        if self.wl.shared_window:  # prefill: each query's causal window over the shared sequence
+            abi.csa2_sparse_attn_prefill(self.attn_q[li], B, self.kv_codes, self.kv_scales, self.n_rows,
+                                         self.kv_start, self.n_visible, idx, self.K, self.swa[li], self.Wn,
+                                         self.sm_scale, self.out[li], self.out_code, self.lse[li], self.ws_attn,
+                                         self.ws_attn.numel(), s)
+            return
         abi.csa2_sparse_attn(self.attn_q[li], B, self.kv_codes, self.kv_scales, self.n_rows, self.kv_start,
                              self.n_visible, idx, self.K, self.swa[li],
                              self.tok_swa[li] if swa_append else None, self.Wn, self.sm_scale,

@@ -22,11 +22,14 @@ import numpy as np
 SEED = 20260910
 
 # stream kinds
-_K_INDEX_Q, _K_INDEX_W, _K_INDEX_K, _K_HOT, _K_LATENT, _K_SWA, _K_ATTN_Q, _K_CTX = range(8)
+_K_INDEX_Q, _K_INDEX_W, _K_INDEX_K, _K_HOT, _K_LATENT, _K_SWA, _K_ATTN_Q, _K_CTX, _K_SWA_SEQ = range(9)
 _CHUNK_ROWS = 8192
 
 FULL, REINDEX, REUSE = "F", "X", "R"
 GROUP_LAYOUT = (FULL, REUSE, REUSE, REUSE) + (REINDEX, REUSE, REUSE, REUSE) * 4
+# [T1] §二 layout paragraph: the encoder's CSA2 layers run at m = 2 in three
+# groups of one Full and five Reuse layers
+ENCODER_LAYOUT = (FULL, REUSE, REUSE, REUSE, REUSE, REUSE) * 3
 
 
 @dataclass(frozen=True)
@@ -49,6 +52,7 @@ class Workload:
     cache_entries: int = 0         # rows of the shared cache (shared_cache only)
     m: int = 1                     # raw tokens per compressed entry
     raw_positions: tuple = ()      # per-query raw position (shared_cache only)
+    shared_window: bool = False    # window over the shared sequence (prefill) instead of a ring per query
     extra: dict = field(default_factory=dict, compare=False)
 
     @property
@@ -97,6 +101,18 @@ def many_query(queries=4096, entries=262144, m=2):
     ctx = tuple((p + 1) // m for p in raw)
     return Workload(f"manyq-{queries}x{entries}-m{m}", 3, ctx, (FULL,),
                     shared_cache=True, cache_entries=entries, m=m, raw_positions=raw)
+
+
+def encoder_m2(queries=4096, entries=262144, m=2):
+    """Encoder-side CSA2 over a prefill chunk: `queries` consecutive raw
+    positions ending at the last raw token, one shared cache of `entries`
+    m=2 entries, layers [Full + 5 Reuse] x 3; each query attends to its
+    top-512 and its own causal window over the shared sequence."""
+    raw_end = entries * m
+    raw = tuple(range(raw_end - queries, raw_end))
+    ctx = tuple((p + 1) // m for p in raw)
+    return Workload(f"encoder-{queries}x{entries}-m{m}-FRRRRRx3", 5, ctx, ENCODER_LAYOUT,
+                    shared_cache=True, cache_entries=entries, m=m, raw_positions=raw, shared_window=True)
 
 
 def ragged(count=64):
@@ -223,6 +239,12 @@ def swa_ring(w: Workload, q, layer):
     [window][512] N(0,1)."""
     x = _rng(w, _K_SWA, q, layer).standard_normal((w.window, 512), dtype=np.float32)
     return to_bf16_exact(x)
+
+
+def swa_seq_rows(w: Workload, layer, r0=0, r1=None):
+    """Rows [r0, r1) of a layer's window latents over the shared sequence
+    (one per compressed position): bf16 [entries][512] N(0,1)."""
+    return to_bf16_exact(_normal_rows(w, _K_SWA_SEQ, (layer,), w.cache_entries, 512, r0, r1))
 
 
 def attn_q(w: Workload, q, layer):

@@ -268,6 +268,26 @@ csa2_status csa2_sparse_attn(const void* q_bf16, int64_t n_q,
                              void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /*
+ * Prefill sparse attention over a shared sequence ([T1] §二 layout paragraph:
+ * the encoder runs CSA2 at m = 2 in groups of one Full and five Reuse
+ * layers, over a prefill chunk of many query tokens).  As csa2_sparse_attn,
+ * except that each query's window is its own causal window over the
+ * sequence the queries share: the last min(window, n) positions p < n of
+ * query t, read from
+ *   swa_rows [n_rows][512] E4M3, row kv_start[t] + p
+ * (the same row numbering as the main latent; one array per layer, written
+ * with csa2_quantize_append CSA2_FMT_FP8), instead of a ring per query.
+ * There is no current-token append.  The workspace is that of
+ * csa2_sparse_attn (CSA2_OP_SPARSE_ATTN).
+ */
+csa2_status csa2_sparse_attn_prefill(const void* q_bf16, int64_t n_q,
+                                     const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_rows,
+                                     const int64_t* kv_start, const int32_t* n_visible,
+                                     const int32_t* topk, int k, const uint8_t* swa_rows, int window,
+                                     float sm_scale, void* out, int out_dtype, float* out_lse,
+                                     void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/*
  * Instrumentation (off by default; the compute path never depends on it).
  * csa2_launch_count: kernels launched through the library by this process.
  * csa2_timer_enable: bracket the next max_launches launches of kernel

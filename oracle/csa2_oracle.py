@@ -353,6 +353,21 @@ def attention_inputs(topk_ids, main_codes, main_scales, swa_ring, n, window=WIND
     return sel, win
 
 
+def attention_inputs_shared_window(topk_ids, main_codes, main_scales, win_rows, n, window=WINDOW):
+    """The latents one prefill attention call sees: as attention_inputs, but
+    the window is the query's own causal window over the shared sequence,
+    the rows of the last min(W, n) positions of win_rows [positions][512]
+    (E4M3 bytes, one row per compressed position).  READING of [T1] §二 (the
+    encoder's layers at m = 2 keep a 128-entry window like the decoder's):
+    each prefill query's window holds the entries just before it in the
+    sequence all the chunk's queries share."""
+    ids = np.asarray(topk_ids)
+    ids = ids[ids >= 0]
+    sel = dequantize_fp4(np.asarray(main_codes)[ids], np.asarray(main_scales)[ids])
+    win = e4m3_decode(np.asarray(win_rows)[window_positions(n, window)])
+    return sel, win
+
+
 # ---------------------------------------------------------------------------
 # One query through a layer group.
 # [T1] §二: decoder layout [Full + 3 Reuse] + 4 x [Reindex + 3 Reuse]; every

@@ -116,7 +116,8 @@ def oracle_query(wl: W.Workload, q, n=None):
         k_real=W.indexer_k_rows(wl, r, 0, n),
         latent_real=W.main_latent_rows(wl, r, 0, n),
         positions=W.latent_positions(wl, r)[:n],
-        swa_real={i: W.swa_ring(wl, q, i) for i in range(len(wl.layers))},
+        swa_real={i: (W.swa_seq_rows(wl, i, 0, n) if wl.shared_window else W.swa_ring(wl, q, i))
+                  for i in range(len(wl.layers))},
         attn_q={i: W.attn_q(wl, q, i) for i in range(len(wl.layers))},
         n=n, pool_blocks=wl.pool_blocks, topk=wl.topk, window=wl.window)
 
@@ -162,7 +163,7 @@ def verify_query(g, wl, q, check_cache=True):
             gt = g.topk[li][q].cpu().numpy()
             if mode == W.FULL:
                 pool_o, top_o, scores, bmax = O.index_full(qdq, inp["index_w"][li], kdq, n, P, K)
-                gp = g.pool[q].cpu().numpy()
+                gp = g.pools[li][q].cpu().numpy()
                 check_selection(gp, pool_o, lambda b: bmax[b], kth_value(bmax, P), f"q{q} pool")
                 check_selection(gt, top_o, lambda p: scores[p], kth_value(scores, K), f"q{q} L{li} top-k")
                 gpu_pool = gp
@@ -174,8 +175,12 @@ def verify_query(g, wl, q, check_cache=True):
         else:
             topk_of[li] = topk_of[W.index_source(wl, li)]
         ring = O.append_swa_fp8(inp["swa_real"][li])
-        assert np.array_equal(g.swa[li][q].cpu().numpy(), ring), "window bytes"
-        sel, win = O.attention_inputs(topk_of[li], lc, ls, ring, n, wl.window)
+        if wl.shared_window:  # the window over the shared sequence: rows [0, n) of the layer's array
+            assert np.array_equal(g.swa[li][:n].cpu().numpy(), ring), "window bytes"
+            sel, win = O.attention_inputs_shared_window(topk_of[li], lc, ls, ring, n, wl.window)
+        else:
+            assert np.array_equal(g.swa[li][q].cpu().numpy(), ring), "window bytes"
+            sel, win = O.attention_inputs(topk_of[li], lc, ls, ring, n, wl.window)
         o_ref, lse_ref = O.sparse_attention(inp["attn_q"][li], sel, win)
         check_attention(bf16_to_f64(g.out[li][q]), o_ref, f"q{q} L{li} attention")
         lse = g.lse[li][q].cpu().numpy()
@@ -242,7 +247,7 @@ def verify_query_at_scale(g, wl, q, cache_sample=2048, seed=7):
         gt = g.topk[li][q].cpu().numpy()
         if mode == W.FULL:
             pool_o, top_o, scores, bmax = O.index_full(qdq, wv, kdq, n, P, K)
-            gp = g.pool[q].cpu().numpy()
+            gp = g.pools[li][q].cpu().numpy()
             check_selection(gp, pool_o, lambda b: bmax[b], kth_value(bmax, P), f"q{q} pool")
             check_selection(gt, top_o, lambda p: scores[p], kth_value(scores, K), f"q{q} L{li} top-k")
             gpu_pool = gp
@@ -268,9 +273,17 @@ def verify_query_at_scale(g, wl, q, cache_sample=2048, seed=7):
     for li in range(len(wl.layers)):
         t = topk_of[li]
         ids = np.where(t >= 0, row_of[np.maximum(t, 0)], -1)
-        ring = O.append_swa_fp8(W.swa_ring(wl, q, li))
-        assert np.array_equal(g.swa[li][q].cpu().numpy(), ring), f"q{q} L{li} window bytes"
-        sel, win = O.attention_inputs(ids, lc, ls, ring, n, wl.window)
+        if wl.shared_window:  # only the window's rows of the shared sequence are drawn and compared
+            w0 = max(0, n - wl.window)
+            rows = O.append_swa_fp8(W.swa_seq_rows(wl, li, w0, n))
+            assert np.array_equal(g.swa[li][w0:n].cpu().numpy(), rows), f"q{q} L{li} window bytes"
+            seq = np.zeros((n, 512), dtype=np.uint8)
+            seq[w0:n] = rows
+            sel, win = O.attention_inputs_shared_window(ids, lc, ls, seq, n, wl.window)
+        else:
+            ring = O.append_swa_fp8(W.swa_ring(wl, q, li))
+            assert np.array_equal(g.swa[li][q].cpu().numpy(), ring), f"q{q} L{li} window bytes"
+            sel, win = O.attention_inputs(ids, lc, ls, ring, n, wl.window)
         o_ref, lse_ref = O.sparse_attention(W.attn_q(wl, q, li), sel, win)
         check_attention(bf16_to_f64(g.out[li][q]), o_ref, f"q{q} L{li} attention")
         lse = g.lse[li][q].cpu().numpy()

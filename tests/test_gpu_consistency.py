@@ -154,46 +154,47 @@ def _digest(t):
     return hashlib.sha256(t.contiguous().cpu().numpy().tobytes()).hexdigest()
 
 
-def test_index_buffers_keep_their_bytes_through_later_layers():
-    """A 20-layer group ([Full + 3 Reuse] + 4 x [Reindex + 3 Reuse]) stepped
-    one layer at a time: the pool is written only by the Full layer, each
-    Full / Reindex top-k buffer only by its own layer, and none of them
-    changes while the later layers (their Reuse layers' attention, the other
-    Reindex layers) run."""
+@pytest.mark.parametrize("encoder", [False, True])
+def test_index_buffers_keep_their_bytes_through_later_layers(encoder):
+    """A 20-layer decoder group ([Full + 3 Reuse] + 4 x [Reindex + 3 Reuse])
+    or an 18-layer encoder group ([Full + 5 Reuse] x 3, m = 2, prefill
+    attention) stepped one layer at a time: each Full layer's pool is written
+    only by that layer, each Full / Reindex top-k buffer only by its own
+    layer, and none of them changes while the later layers (their Reuse
+    layers' attention, the other Full and Reindex layers) run."""
     from csa2_sparse_attention_gb300.layer_group import LayerGroup
-    wl = W.small_variant(W.group_128k(), (12000, 9000, 16384, 20000), name="ownership", hot_blocks=8)
+    if encoder:
+        wl = W.encoder_m2(queries=64, entries=40000)
+    else:
+        wl = W.small_variant(W.group_128k(), (12000, 9000, 16384, 20000), name="ownership", hot_blocks=8)
     g = LayerGroup(wl)
     g.fill()
     for ws in (g.ws_app, g.ws_full, g.ws_re, g.ws_attn):
         ws.zero_()
     s = torch.cuda.current_stream()
-    g.append_token(s)
-    owned = {}      # buffer name -> digest when its owning layer finished
-    pool_digest = None
+    if not wl.shared_cache:
+        g.append_token(s)
+    buffers = [(f"topk{i}", g.topk[i]) for i in g.index_layers] + [(f"pool{i}", t) for i, t in g.pools.items()]
+    owned = {}  # buffer name -> digest when its owning layer finished
     for li, mode in enumerate(wl.layers):
-        before = {name: _digest(t) for name, t in
-                  [(f"topk{i}", g.topk[i]) for i in g.index_layers] + [("pool", g.pool)]}
-        g.layer(li, s)
+        before = {name: _digest(t) for name, t in buffers}
+        g.layer(li, s, swa_append=not wl.shared_cache)
         torch.cuda.synchronize()
-        after = {name: _digest(t) for name, t in
-                 [(f"topk{i}", g.topk[i]) for i in g.index_layers] + [("pool", g.pool)]}
+        after = {name: _digest(t) for name, t in buffers}
         changed = {name for name in after if after[name] != before[name]}
         # only the layer's own buffers may change
         allowed = set()
         if mode == W.FULL:
-            allowed = {f"topk{li}", "pool"}
+            allowed = {f"topk{li}", f"pool{li}"}
         elif mode == W.REINDEX:
             allowed = {f"topk{li}"}
         assert changed <= allowed, f"layer {li} ({mode}) wrote {sorted(changed - allowed)}"
-        if mode in (W.FULL, W.REINDEX):
-            assert f"topk{li}" in changed, f"layer {li} left its top-k unwritten"
-            owned[f"topk{li}"] = after[f"topk{li}"]
-        if mode == W.FULL:
-            pool_digest = after["pool"]
+        for name in allowed:
+            assert name in changed, f"layer {li} left {name} unwritten"
+            owned[name] = after[name]
         # every buffer owned by an earlier layer still has its bytes
         for name, d in owned.items():
             assert after[name] == d, f"{name} changed during layer {li}"
-        assert after["pool"] == pool_digest
         # the attention of this layer read its index source's buffer
         assert g.attn_index[li] is g.topk[W.index_source(wl, li)]
     for name, st in g.status().items():

@@ -261,3 +261,26 @@ def test_decode_group_reuse_layers_share_indices():
     assert set((out["topk"][2] // 8).tolist()) <= set(out["pool"].tolist())
     for i in range(4):
         assert out["o"][i].shape == (64, 512) and np.all(np.isfinite(out["o"][i]))
+
+
+def test_shared_sequence_window_is_the_ring_window_of_the_same_positions():
+    """The prefill window (rows of the shared sequence) selects exactly the
+    latents a decode ring holding the same last positions selects, so the
+    prefill attention reduces to the pinned ring definition; a context
+    shorter than the window takes all of its positions."""
+    rng = np.random.default_rng(17)
+    W_ = 128
+    for n in (1, 77, 128, 129, 1000):
+        win_rows = rng.integers(0, 0x7F, (n, 512)).astype(np.uint8)  # finite E4M3 bytes
+        win_rows[:, ::3] |= 0x80
+        ring = np.zeros((W_, 512), dtype=np.uint8)
+        for p in range(max(0, n - W_), n):
+            ring[p % W_] = win_rows[p]
+        codes = rng.integers(0, 16, (n, 512))
+        scales = rng.integers(0x30, 0x40, (n, 32)).astype(np.uint8)
+        topk = np.array([0, n - 1, -1, n // 2])
+        sel_a, win_a = O.attention_inputs(topk, codes, scales, ring, n, W_)
+        sel_b, win_b = O.attention_inputs_shared_window(topk, codes, scales, win_rows, n, W_)
+        assert np.array_equal(sel_a, sel_b) and np.array_equal(win_a, win_b)
+        assert win_b.shape[0] == min(n, W_)
+        assert np.array_equal(win_b, O.e4m3_decode(win_rows[max(0, n - W_):n]))
