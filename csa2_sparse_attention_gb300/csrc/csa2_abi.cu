@@ -111,12 +111,12 @@ extern "C" csa2_status csa2_status_fetch(const void* ws, int32_t out[4], csa2_st
 
 extern "C" int64_t csa2_launch_count(void) { return g_launches.load(); }
 
+static std::atomic<uint64_t> g_wait_ns{2000000000ull};
+uint64_t csa2::wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 extern "C" csa2_status csa2_debug_wait_limit(int64_t ns) {
     if (ns < 0) return CSA2_ERR_INVALID_ARG;
-    if (set_wait_limit_index(uint64_t(ns)) != cudaSuccess || set_wait_limit_attn(uint64_t(ns)) != cudaSuccess) {
-        cudaGetLastError();
-        return CSA2_ERR_CUDA;
-    }
+    g_wait_ns.store(ns == 0 ? 2000000000ull : uint64_t(ns), std::memory_order_relaxed);
     return CSA2_OK;
 }
 

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const int32_t* __restrict__ n_visible, const int32_t* __restrict__ topk, int k,
     uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, bool win_shared, float sm_scale,
     float* __restrict__ part_o, float* __restrict__ part_ml, int splits, void* __restrict__ out,
-    bool out_f32, float* __restrict__ out_lse, Status* st) {
+    bool out_f32, float* __restrict__ out_lse, Status* st, uint64_t wlim) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     AttnTcSmem& S = *reinterpret_cast<AttnTcSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     // them in flight: the CTA then writes nothing more into C or the Q/P
     // area (their operands), takes part in the cluster barriers only, and
     // waits for them once more before TMEM is released.
-    bool ok_mma = __syncthreads_and(mbar_wait(&S.bar, 0));
+    bool ok_mma = __syncthreads_and(mbar_wait(&S.bar, 0, wlim));
     uint32_t pending = ok_mma ? 0u : 1u;  // 1 + the parity of the MMA commit still outstanding
     tc_fence_after();
 
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         tc_commit(&S.bar);
     }
     if (ok_mma) {
-        ok_mma = __syncthreads_and(mbar_wait(&S.bar, 1));
+        ok_mma = __syncthreads_and(mbar_wait(&S.bar, 1, wlim));
         if (!ok_mma) pending = 2u;
     }
     tc_fence_after();
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         }
         cluster.sync();  // peers are done reading this CTA's shared memory
     }
-    if (tid == 0 && pending != 0) mbar_wait(&S.bar, pending - 1, 100000000ull);
+    if (tid == 0 && pending != 0) mbar_wait(&S.bar, pending - 1, kDrainNs);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTcCols);
@@ -620,9 +620,6 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     if (lse && lane == 0) lse[q * kH + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
-// The bounded waits' limit of this unit's kernels (a test hook).
-cudaError_t set_wait_limit_attn(uint64_t ns) { return set_wait_limit(ns); }
-
 // Opt both variants into their shared memory and note how many clusters of
 // `splits` CTAs can be resident at once (0 when clusters are unavailable).
 static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
@@ -704,10 +701,10 @@ static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* k
     const cudaError_t le =
         cluster ? launch(attn_tc_kernel<true>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
                          kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
-                         sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st)
+                         sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns())
                 : launch(attn_tc_kernel<false>, grid, kAttnThreads, sizeof(AttnTcSmem), s, 1, q, kv_codes,
                          kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared, sm_scale,
-                         part_o, part_ml, L.splits, out, f32, out_lse, st);
+                         part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns());
     timer_end(K_ATTN_SPLIT, s);
     if (le != cudaSuccess) return CSA2_ERR_CUDA;
     if (cluster) return launch_status();

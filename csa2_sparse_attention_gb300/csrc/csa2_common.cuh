@@ -147,8 +147,7 @@ namespace csa2 {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 csa2_status launch_status();  // maps cudaGetLastError to a csa2_status
 int sm_count();               // the current device's multiprocessors (queried once per device)
-cudaError_t set_wait_limit_index(uint64_t ns);  // the bounded waits' limit, per translation unit
-cudaError_t set_wait_limit_attn(uint64_t ns);
+uint64_t wait_limit_ns();      // the bounded waits' limit, passed to every launch (2 s by default)
 
 // Launches `kernel` on `s` with programmatic stream serialization (see
 // grid_dep_wait) and, when cluster > 1, clusters of `cluster` CTAs along x.

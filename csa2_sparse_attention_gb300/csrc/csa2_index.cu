@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const uint8_t* __restrict__ k_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, const int32_t* __restrict__ cand,
     int64_t cand_stride, int C, float* __restrict__ out, int64_t out_stride, int ctas_per_query,
-    bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride) {
+    bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride, uint64_t wlim) {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
     const bool rec = k_scales == nullptr;  // indexer K as 576-byte records
@@ -277,8 +277,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         }
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % kTcStages, r = i / kTcStages;
-            int ok = *reinterpret_cast<volatile int*>(&S.abort_flag) == 0;
-            if (ok && lane == 0 && r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1)) {
+            int ok = 1;
+            if (lane == 0 && r > 0 && !mbar_wait(&S.empty[s], (r - 1) & 1, wlim)) {
                 record(st, CSA2_ERR_TIMEOUT, 10, int32_t(q), i);
                 S.abort_flag = 1;
                 ok = 0;
@@ -324,13 +324,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         }
     } else if (warp == 1) {  // ----------------------------------- MMA issue
         if (lane == 0) {
-            bool ok = mbar_wait(&S.qbar, 0);
+            bool ok = mbar_wait(&S.qbar, 0, wlim);
             constexpr uint32_t id = idesc_mxf4nvf4(128, 32);
             const uint32_t qa = smem_u32(S.qcodes);
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int s = i % kTcStages, f = i % kTcSf, a = i % kTcAcc;
-                ok = mbar_wait(&S.full[s], (i / kTcStages) & 1) && mbar_wait(&S.sfa_ready[f], (i / kTcSf) & 1) &&
-                     (i < kTcAcc || mbar_wait(&S.acc_empty[a], ((i / kTcAcc) - 1) & 1));
+                ok = mbar_wait(&S.full[s], (i / kTcStages) & 1, wlim) && mbar_wait(&S.sfa_ready[f], (i / kTcSf) & 1, wlim) &&
+                     (i < kTcAcc || mbar_wait(&S.acc_empty[a], ((i / kTcAcc) - 1) & 1, wlim));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(S.stage[s]), sbo = rec ? 576 : 512;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         }
         auto stage_sf = [&](int i) -> bool {  // tile i's scales (A) into slot i % kTcSf
             const int s = i % kTcStages, f = i % kTcSf;
-            if (!mbar_wait(&S.full[s], (i / kTcStages) & 1)) return false;
+            if (!mbar_wait(&S.full[s], (i / kTcStages) & 1, wlim)) return false;
             uint2 r4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -376,15 +376,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         bool ok = true;
         for (int i = 0; ok && i < kTcSfLead && i < ntiles; ++i) ok = stage_sf(i);
         for (int i = 0; ok && i < ntiles; ++i) {
-            if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
-                ok = false;
-                break;
-            }
             // tile i + lead reuses the slot of tile i + lead - kTcSf, whose MMA
             // finished before tile i - 1's accumulator was read
             if (i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
             const int a = i % kTcAcc;
-            if (!ok || !mbar_wait(&S.acc_full[a], (i / kTcAcc) & 1)) {
+            if (!ok || !mbar_wait(&S.acc_full[a], (i / kTcAcc) & 1, wlim)) {
                 ok = false;
                 break;
             }
@@ -423,19 +419,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     }
     tc_fence_before();
     __syncthreads();
-    if (S.abort_flag && lane == 0) {
+    if (S.abort_flag) {  // (uniform: nothing writes the flag after the barrier)
         // a wait gave up: wait for the copies and MMAs already issued (the
         // last commit covers every earlier MMA) before anything is released
-        if (warp == 0) {
+        if (lane == 0 && warp == 0) {
             mbar_wait(&S.qbar, 0, kDrainNs);
             for (int i = issued > kTcStages ? issued - kTcStages : 0; i < issued; ++i)
                 mbar_wait(&S.full[i % kTcStages], (i / kTcStages) & 1, kDrainNs);
-        } else if (warp == 1 && mma_n > 0) {
+        } else if (lane == 0 && warp == 1 && mma_n > 0) {
             mbar_wait(&S.empty[(mma_n - 1) % kTcStages], ((mma_n - 1) / kTcStages) & 1, kDrainNs);
         }
+        tc_fence_before();
+        __syncthreads();
     }
-    tc_fence_before();
-    __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, kTcCols);
 }
 
@@ -1303,7 +1299,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales, const float* __restrict__ w,
     const uint8_t* __restrict__ k_codes, const uint8_t* __restrict__ k_scales, int64_t n_rows,
     const int64_t* __restrict__ kv_start, const int32_t* __restrict__ n_visible, int32_t max_visible, int64_t n_q,
-    float* __restrict__ out, int64_t out_stride, Status* st) {
+    float* __restrict__ out, int64_t out_stride, Status* st, uint64_t wlim) {
     extern __shared__ __align__(1024) uint8_t mq_smem_raw[];
     MqSmem& S = *reinterpret_cast<MqSmem*>(mq_smem_raw);
     const bool rec = k_scales == nullptr;  // indexer K as 576-byte records
@@ -1370,7 +1366,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                     ++q_copies;
                     for (int i = 0; i < ntiles; ++i) {
                         const int g = it + i, s = g % kTcStages, rr = g / kTcStages;
-                        if (rr > 0 && !mbar_wait(&S.empty[s], (rr - 1) & 1)) {
+                        if (rr > 0 && !mbar_wait(&S.empty[s], (rr - 1) & 1, wlim)) {
                             record(st, CSA2_ERR_TIMEOUT, 20, int32_t(q0 + r0), i);
                             S.abort_flag = 1;
                             break;
@@ -1391,14 +1387,14 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                 }
             } else if (warp == 1) {  // --------------------------- MMA issue
                 if (lane == 0) {
-                    bool ok = mbar_wait(&S.qbar, run & 1);
+                    bool ok = mbar_wait(&S.qbar, run & 1, wlim);
                     const uint32_t id = idesc_mxf4nvf4(128, 32 * nr);
                     const uint32_t qa = smem_u32(S.qcodes);
                     for (int i = 0; ok && i < ntiles; ++i) {
                         const int g = it + i, s = g % kTcStages, f = g % kTcSf;
                         const int a = g % kMqAcc;
-                        ok = mbar_wait(&S.full[s], (g / kTcStages) & 1) && mbar_wait(&S.sfa_ready[f], (g / kTcSf) & 1) &&
-                             (g < kMqAcc || mbar_wait(&S.acc_empty[a], ((g / kMqAcc) - 1) & 1));
+                        ok = mbar_wait(&S.full[s], (g / kTcStages) & 1, wlim) && mbar_wait(&S.sfa_ready[f], (g / kTcSf) & 1, wlim) &&
+                             (g < kMqAcc || mbar_wait(&S.acc_empty[a], ((g / kMqAcc) - 1) & 1, wlim));
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t ka = smem_u32(S.stage[s]), sbo = rec ? 576 : 512;
@@ -1437,7 +1433,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                 }
                 auto stage_sf = [&](int i) -> bool {
                     const int g = it + i, s = g % kTcStages, f = g % kTcSf;
-                    if (!mbar_wait(&S.full[s], (g / kTcStages) & 1)) return false;
+                    if (!mbar_wait(&S.full[s], (g / kTcStages) & 1, wlim)) return false;
                     uint2 r4[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
@@ -1458,7 +1454,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                 for (int i = 0; ok && i < ntiles; ++i) {
                     if (stager && i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
                     const int g = it + i, a = g % kMqAcc;
-                    if (!ok || !mbar_wait(&S.acc_full[a], (g / kMqAcc) & 1)) {
+                    if (!ok || !mbar_wait(&S.acc_full[a], (g / kMqAcc) & 1, wlim)) {
                         ok = false;
                         break;
                     }
@@ -1500,19 +1496,19 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     }
     tc_fence_before();
     __syncthreads();
-    if (S.abort_flag && lane == 0) {
+    if (S.abort_flag) {  // (uniform: nothing writes the flag after the barrier)
         // a wait gave up: wait for the copies and MMAs already issued (the
         // last commit covers every earlier MMA) before anything is released
-        if (warp == 0) {
+        if (lane == 0 && warp == 0) {
             if (q_copies > 0) mbar_wait(&S.qbar, (q_copies - 1) & 1, kDrainNs);
             for (int g = issued > kTcStages ? issued - kTcStages : 0; g < issued; ++g)
                 mbar_wait(&S.full[g % kTcStages], (g / kTcStages) & 1, kDrainNs);
-        } else if (warp == 1 && mma_n > 0) {
+        } else if (lane == 0 && warp == 1 && mma_n > 0) {
             mbar_wait(&S.empty[(mma_n - 1) % kTcStages], ((mma_n - 1) / kTcStages) & 1, kDrainNs);
         }
+        tc_fence_before();
+        __syncthreads();
     }
-    tc_fence_before();
-    __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, kMqCols);
 }
 
@@ -1561,9 +1557,6 @@ static csa2_status prepare_select_kernels() {
     done[dev] = true;
     return CSA2_OK;
 }
-
-// The bounded waits' limit of this unit's kernels (a test hook).
-cudaError_t set_wait_limit_index(uint64_t ns) { return set_wait_limit(ns); }
 
 // CTAs per query for a tensor-core scorer launch: two resident CTAs per SM
 // over the whole batch, at most one per tile.
@@ -1622,7 +1615,7 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
         timer_begin(K_POOL_SCORE, s);
         launch(score_tc_kernel<true>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand, cand_stride, C,
-            scores, score_stride, int(cpq), check_cand, st, nullptr, int64_t(0));
+            scores, score_stride, int(cpq), check_cand, st, nullptr, int64_t(0), wait_limit_ns());
         timer_end(K_POOL_SCORE, s);
     }
     const int cap_t = sel_cap(8 * int64_t(C));
@@ -1667,7 +1660,7 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         timer_begin(K_SCAN, s);
         launch(scan_mq_kernel, dim3(unsigned(chunks), unsigned(groups)), kMqThreads, sizeof(MqSmem), s, 1, q_codes,
                q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, n_q, blockmax, L.nb_stride,
-               st);
+               st, wait_limit_ns());
         timer_end(K_SCAN, s);
     } else if (max_visible > 0) {
         const int64_t cpq = tc_ctas_per_query(n_q, ceil_div<int64_t>(max_visible, kTile));
@@ -1676,7 +1669,7 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         launch(score_tc_kernel<false>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0,
             (n_q <= kScanMaxQ && n_q <= sm_count()) ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st,
-            L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride);
+            L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride, wait_limit_ns());
         timer_end(K_SCAN, s);
     }
     launch_select_blocks(blockmax, L.nb_stride, n_q, kv_start, n_visible, max_visible, n_rows, pool_blocks,

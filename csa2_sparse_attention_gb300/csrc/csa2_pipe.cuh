@@ -5,7 +5,6 @@
 #pragma once
 
 #include <cstdint>
-#include <cuda_runtime.h>
 
 namespace csa2 {
 
@@ -44,54 +43,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
     return ok != 0;
 }
 
-// One non-blocking test of the phase.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// Time limit of the bounded waits: 2 s, unless a test of the give-up paths
-// shortens it (csa2_debug_wait_limit).  One copy per translation unit, set
-// through that unit's set_wait_limit().
-static __device__ uint64_t g_wait_limit_ns = 2000000000ull;
 // Waits that drain copies and MMAs already issued after a give-up use their
-// own limit, which the test hook does not shorten.
+// own limit, which the test hook (csa2_debug_wait_limit) does not shorten.
 constexpr uint64_t kDrainNs = 100000000ull;
 
 // Wait for the completion of the barrier phase with the given parity; gives
-// up after about `limit_ns` nanoseconds (0: the unit's wait limit).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 0) {
-    if (limit_ns == 0) limit_ns = g_wait_limit_ns;
-    if (limit_ns < 1000000u) {  // a short (test) limit: poll without suspending, so it is kept
-        const uint64_t t0 = global_ns();
-        while (!mbar_test_wait(bar, parity)) {
-            if (global_ns() - t0 > limit_ns) return false;
-        }
-        return true;
-    }
-    if (mbar_try_wait(bar, parity)) return true;
+// up after about `limit_ns` nanoseconds.  Kernels take the limit as a launch
+// argument: 2 s, unless a test of the give-up paths passes a limit under
+// 1 ms, which makes every such wait give up at once.  (Any second wait form
+// in the loop -- a polling test_wait, even predicated off -- slowed the
+// decode scan by 7%, so the test form only masks the result.)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    const bool give_up = limit_ns < 1000000u;
+    if (mbar_try_wait(bar, parity) & !give_up) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > limit_ns) return false;
+    for (;;) {
+        if (give_up | (global_ns() - t0 > limit_ns)) return false;
+        if (mbar_try_wait(bar, parity)) return true;
     }
-    return true;
-}
-
-// Host: this translation unit's wait limit (0 restores 2 s).
-static inline cudaError_t set_wait_limit(uint64_t ns) {
-    const uint64_t v = ns == 0 ? 2000000000ull : ns;
-    return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof v);
 }
 
 // One bulk copy global -> shared memory that completes `bytes` of the

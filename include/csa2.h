@@ -305,10 +305,12 @@ int64_t csa2_launch_count(void);
  * a barrier (copies arriving, MMAs completing) is bounded: after 2 s it
  * records CSA2_ERR_TIMEOUT in the status word, stops issuing work, waits for
  * the copies and MMAs it already started, and returns.  csa2_debug_wait_limit
- * sets that limit (in nanoseconds) for kernels launched afterwards on the
- * current device; 0 restores 2 s.  A short limit makes the waits give up on
- * purpose, so a test can check the status and that the next normal call is
- * correct.  Not for production use and not during stream capture.
+ * sets that limit (in nanoseconds) for kernels launched afterwards, on every
+ * device (it is a launch argument: a graph captured earlier keeps the limit
+ * it was captured with); 0 restores 2 s.  A limit under 1 ms makes every
+ * bounded wait give up at once, so a test can check the status, that the
+ * copies and MMAs in flight were waited for, and that the next normal call
+ * is correct.  Not for production use and not during stream capture.
  */
 csa2_status csa2_debug_wait_limit(int64_t ns);
 const char* csa2_kernel_name(int kernel_id);

@@ -2,11 +2,12 @@
 CSA2_ERR_TIMEOUT, the kernel waits for the copies and MMAs it already
 started, and the next normal call is correct.
 
-The test shortens every library wait to 1 ns (csa2_debug_wait_limit), so the
-waits on copies and MMAs in flight give up at once, in the decode scan, the
-pool scoring and the attention kernel; nothing is left waiting on a flag that
-no one sets, and no device fault is involved.  With the limit restored, the
-same step gives the same bytes as before.
+The test sets the library's wait limit to 1 ns (csa2_debug_wait_limit; any
+limit under 1 ms makes every bounded wait give up at once), so the waits on
+copies and MMAs in flight give up in the decode scan, the pool scoring, the
+many-query scan and the attention kernel; nothing is left waiting on a flag
+that no one sets, and no device fault is involved.  With the limit restored,
+the same step gives the same bytes as before.
 """
 import numpy as np
 import pytest
