@@ -61,7 +61,7 @@ class LayerGroup:
     """Caches, per-layer inputs/outputs and workspaces of one workload."""
 
     def __init__(self, wl: W.Workload, device="cuda", sm_scale=1.0 / math.sqrt(512.0),
-                 rope_theta=10000.0, out_dtype=torch.float32, ik_layout=abi.LAYOUT_BLOCK8R):
+                 rope_theta=10000.0, out_dtype=torch.float32, ik_layout=None):
         self.wl = wl
         self.dev = torch.device(device)
         self.B = wl.batch
@@ -87,7 +87,14 @@ class LayerGroup:
         self.kv_codes = torch.zeros((self.n_rows, 256), dtype=u8, device=d)
         self.kv_scales = torch.zeros((self.n_rows, 32), dtype=u8, device=d)
         # indexer K: 576-byte records of 8 rows (codes then scales), or BLOCK8
-        # codes with a separate scale plane
+        # codes with a separate scale plane.  By default decode caches use the
+        # records (the pool gather reads a block in one copy) and shared
+        # prefill caches the split form: the many-query scan's 128-row MMA
+        # operand then has its 8-row groups on 128-byte boundaries (512 B
+        # apart instead of 576), and that scan, bound by its epilogue and MMA
+        # issue rather than by memory, runs faster on it.
+        if ik_layout is None:
+            ik_layout = abi.LAYOUT_BLOCK8 if wl.shared_cache else abi.LAYOUT_BLOCK8R
         self.ik_layout = ik_layout
         if ik_layout == abi.LAYOUT_BLOCK8R:
             self.ik_codes = torch.zeros((self.n_rows // 8 * 576,), dtype=u8, device=d)
