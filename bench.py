@@ -627,8 +627,8 @@ def run_e2e(g, stream, flush, K, wl):
 
 
 # ----------------------------------------------------------- ncu launch list
-NCU_NAMES = (("score_tc_kernel<false>", "scan_blockmax"), ("score_tc_kernel<true>", "pool_score"),
-             ("score_tc_kernel<0>", "scan_blockmax"), ("score_tc_kernel<1>", "pool_score"),
+NCU_NAMES = (("score_tc_kernel<false", "scan_blockmax"), ("score_tc_kernel<true", "pool_score"),
+             ("score_tc_kernel<0", "scan_blockmax"), ("score_tc_kernel<1", "pool_score"),
              ("select_blocks_kernel", "select_blocks"), ("select_blocks_cluster_kernel", "select_blocks"),
              ("select_topk_kernel", "select_topk"),
              ("attn_tc_kernel", "attn_split"), ("attn_merge_kernel", "attn_merge"),

@@ -77,17 +77,22 @@ static_assert(kTcMaxCandPerCta >= kMaxPoolBlocks, "a CTA stages at most all cand
 
 // Indexer K arrives either as BLOCK8 code blocks of 512 bytes with the
 // scales in their own row-major plane, or as 576-byte records (a block's 512
-// code bytes, then its 8 rows x 8 scale bytes).  A stage holds one tile in
-// the same form: 16 x 512 code bytes then 16 x 64 scale bytes, or 16
-// records; the MMA reads the codes in place (8-row groups 512 or 576 bytes
-// apart).
+// code bytes, then its 8 rows x 8 scale bytes).  A stage of the ring holds
+// one tile in the same form: 16 records, or 16 x 512 code bytes then 16 x 64
+// scale bytes.  The MMA reads the codes in place (8-row groups 576 or 512
+// bytes apart).
 constexpr int kStageBytes = kTile * 72;
-__device__ __forceinline__ uint32_t stage_scale_off(bool rec, int row) {
-    return rec ? uint32_t((row >> 3) * 576 + 512 + (row & 7) * 8) : uint32_t(kTile * 64 + row * 8);
+template <bool REC>
+__device__ __forceinline__ uint8_t* stage_codes(uint8_t* ring, int s) {
+    return ring + s * kStageBytes;
+}
+template <bool REC>
+__device__ __forceinline__ uint8_t* stage_scales(uint8_t* ring, int s, int row) {
+    return ring + s * kStageBytes + (REC ? (row >> 3) * 576 + 512 + (row & 7) * 8 : kTile * 64 + row * 8);
 }
 
 struct TcScanSmem {
-    uint8_t stage[kTcStages][kStageBytes];
+    uint8_t ring[kTcStages * kStageBytes];
     uint8_t qcodes[32 * 64];          // the query's 32 heads, BLOCK8 = canonical K-major
     int32_t cand[kTcMaxCandPerCta];   // this CTA's candidate blocks (pool scoring)
     uint64_t full[kTcStages], empty[kTcStages];
@@ -189,7 +194,7 @@ __device__ bool scan_map(const int64_t* kv_start, const int32_t* n_visible, int3
     return q >= 0;
 }
 
-template <bool GATHER>
+template <bool GATHER, bool REC>
 __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales,
     const float* __restrict__ w, const uint8_t* __restrict__ k_codes,
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride, uint64_t wlim) {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
-    const bool rec = k_scales == nullptr;  // indexer K as 576-byte records
+    constexpr bool rec = REC;  // indexer K as 576-byte records (k_scales unused)
     grid_dep_wait();
     grid_dep_launch();
     int64_t q = blockIdx.y, t0, t1;
@@ -291,10 +296,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                     const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
                     mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
                     if (rec) {
-                        bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 576, nvb * 576, &S.full[s]);
+                        bulk_g2s(stage_codes<rec>(S.ring, s), k_codes + ((ks >> 3) + t * 16) * 576, nvb * 576,
+                                 &S.full[s]);
                     } else {
-                        bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
-                        bulk_g2s(S.stage[s] + kTile * 64, k_scales + (ks + t * kTile) * 8, nvb * 64, &S.full[s]);
+                        bulk_g2s(stage_codes<rec>(S.ring, s), k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512,
+                                 &S.full[s]);
+                        bulk_g2s(stage_scales<rec>(S.ring, s, 0), k_scales + (ks + t * kTile) * 8, nvb * 64,
+                                 &S.full[s]);
                     }
                 }
                 issued = i + 1;
@@ -312,11 +320,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                 __syncwarp();
                 if (live) {
                     if (rec)
-                        bulk_g2s(S.stage[s] + j * 576, k_codes + ((ks >> 3) + bl) * 576, 576, &S.full[s]);
+                        bulk_g2s(stage_codes<rec>(S.ring, s) + j * 576, k_codes + ((ks >> 3) + bl) * 576, 576,
+                                 &S.full[s]);
                     else if (lane < 16)
-                        bulk_g2s(S.stage[s] + j * 512, k_codes + ((ks >> 3) + bl) * 512, 512, &S.full[s]);
+                        bulk_g2s(stage_codes<rec>(S.ring, s) + j * 512, k_codes + ((ks >> 3) + bl) * 512, 512,
+                                 &S.full[s]);
                     else
-                        bulk_g2s(S.stage[s] + kTile * 64 + j * 64, k_scales + (ks + 8 * int64_t(bl)) * 8, 64,
+                        bulk_g2s(stage_scales<rec>(S.ring, s, 8 * j), k_scales + (ks + 8 * int64_t(bl)) * 8, 64,
                                  &S.full[s]);
                 }
                 issued = i + 1;
@@ -333,7 +343,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                      (i < kTcAcc || mbar_wait(&S.acc_empty[a], ((i / kTcAcc) - 1) & 1, wlim));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t ka = smem_u32(S.stage[s]), sbo = rec ? 576 : 512;
+                const uint32_t ka = smem_u32(stage_codes<rec>(S.ring, s)), sbo = rec ? 576 : 512;
                 const uint32_t d = tmem + kColAcc + 32 * a;
                 const uint32_t sfa = tmem + kColSfa + 8 * f, sfb = tmem + kColSfb;
                 mma_mxf4_ss(d, umma_desc(ka, 128, sbo), umma_desc(qa, 128, 512), id, sfa, sfb, false);
@@ -365,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
             uint2 r4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                r4[j] = *reinterpret_cast<const uint2*>(S.stage[s] + stage_scale_off(rec, lane + 32 * j));
+                r4[j] = *reinterpret_cast<const uint2*>(stage_scales<rec>(S.ring, s, lane + 32 * j));
             tmem_st4(lane_base + kColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
             tmem_st4(lane_base + kColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
             tmem_st_wait();
@@ -1283,7 +1293,7 @@ constexpr uint32_t kMqCols = 512;
 constexpr uint32_t kMqColSfa = 256, kMqColSfb = 288;  // scale slots (4 x 8 columns), query scales (8)
 
 struct MqSmem {
-    uint8_t stage[kTcStages][kStageBytes];
+    uint8_t ring[kTcStages * kStageBytes];
     uint8_t qcodes[kMqQ * 32 * 64];  // the run's query heads, BLOCK8 = canonical K-major
     float w[kMqQ * 32];
     int32_t n[kMqQ];
@@ -1295,6 +1305,7 @@ struct MqSmem {
     int abort_flag;
 };
 
+template <bool REC>
 __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales, const float* __restrict__ w,
     const uint8_t* __restrict__ k_codes, const uint8_t* __restrict__ k_scales, int64_t n_rows,
@@ -1302,7 +1313,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
     float* __restrict__ out, int64_t out_stride, Status* st, uint64_t wlim) {
     extern __shared__ __align__(1024) uint8_t mq_smem_raw[];
     MqSmem& S = *reinterpret_cast<MqSmem*>(mq_smem_raw);
-    const bool rec = k_scales == nullptr;  // indexer K as 576-byte records
+    constexpr bool rec = REC;  // indexer K as 576-byte records (k_scales unused)
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
     const int64_t q0 = int64_t(blockIdx.y) * kMqQ;
     const int nqg = int(n_q - q0 < kMqQ ? n_q - q0 : kMqQ);
@@ -1376,10 +1387,12 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                         const uint32_t nvb = uint32_t(nvb64 < 16 ? nvb64 : 16);
                         mbar_arrive_expect_tx(&S.full[s], nvb * (512 + 64));
                         if (rec) {
-                            bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 576, nvb * 576, &S.full[s]);
+                            bulk_g2s(stage_codes<rec>(S.ring, s), k_codes + ((ks >> 3) + t * 16) * 576, nvb * 576,
+                                     &S.full[s]);
                         } else {
-                            bulk_g2s(S.stage[s], k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512, &S.full[s]);
-                            bulk_g2s(S.stage[s] + kTile * 64, k_scales + (ks + t * kTile) * 8, nvb * 64,
+                            bulk_g2s(stage_codes<rec>(S.ring, s), k_codes + ((ks >> 3) + t * 16) * 512, nvb * 512,
+                                     &S.full[s]);
+                            bulk_g2s(stage_scales<rec>(S.ring, s, 0), k_scales + (ks + t * kTile) * 8, nvb * 64,
                                      &S.full[s]);
                         }
                         issued = g + 1;
@@ -1397,7 +1410,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                              (g < kMqAcc || mbar_wait(&S.acc_empty[a], ((g / kMqAcc) - 1) & 1, wlim));
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t ka = smem_u32(S.stage[s]), sbo = rec ? 576 : 512;
+                        const uint32_t ka = smem_u32(stage_codes<rec>(S.ring, s)), sbo = rec ? 576 : 512;
                         const uint32_t d = tmem + 128 * a;
                         const uint32_t sfa = tmem + kMqColSfa + 8 * f, sfb = tmem + kMqColSfb;
                         mma_mxf4_ss(d, umma_desc(ka, 128, sbo), umma_desc(qa, 128, 512), id, sfa, sfb, false);
@@ -1437,7 +1450,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
                     uint2 r4[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        r4[j] = *reinterpret_cast<const uint2*>(S.stage[s] + stage_scale_off(rec, lane + 32 * j));
+                        r4[j] = *reinterpret_cast<const uint2*>(stage_scales<rec>(S.ring, s, lane + 32 * j));
                     tmem_st4(lane_base + kMqColSfa + 8 * f, r4[0].x, r4[1].x, r4[2].x, r4[3].x);
                     tmem_st4(lane_base + kMqColSfa + 8 * f + 4, r4[0].y, r4[1].y, r4[2].y, r4[3].y);
                     tmem_st_wait();
@@ -1541,12 +1554,14 @@ static csa2_status prepare_select_kernels() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
     if (done[dev]) return CSA2_OK;
     const int bytes = (kSelSmemKeys + kMaxPoolBlocks) * 4;
-    if (cudaFuncSetAttribute(score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(sizeof(TcScanSmem))) != cudaSuccess ||
-        cudaFuncSetAttribute(score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(sizeof(TcScanSmem))) != cudaSuccess ||
-        cudaFuncSetAttribute(scan_mq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(sizeof(MqSmem))) != cudaSuccess ||
+    const int tc = int(sizeof(TcScanSmem)), mq = int(sizeof(MqSmem));
+    const auto smem = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (cudaFuncSetAttribute(score_tc_kernel<false, false>, smem, tc) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel<false, true>, smem, tc) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel<true, false>, smem, tc) != cudaSuccess ||
+        cudaFuncSetAttribute(score_tc_kernel<true, true>, smem, tc) != cudaSuccess ||
+        cudaFuncSetAttribute(scan_mq_kernel<false>, smem, mq) != cudaSuccess ||
+        cudaFuncSetAttribute(scan_mq_kernel<true>, smem, mq) != cudaSuccess ||
         cudaFuncSetAttribute(select_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(select_blocks_cluster_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1613,9 +1628,10 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
         const int64_t cpq = tc_ctas_per_query(n_q, (C + 15) / 16);
         const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
         timer_begin(K_POOL_SCORE, s);
-        launch(score_tc_kernel<true>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
-            q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand, cand_stride, C,
-            scores, score_stride, int(cpq), check_cand, st, nullptr, int64_t(0), wait_limit_ns());
+        launch(k_scales == nullptr ? score_tc_kernel<true, true> : score_tc_kernel<true, false>, grid, kTcThreads,
+            sizeof(TcScanSmem), s, 1, q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible,
+            max_visible, cand, cand_stride, C, scores, score_stride, int(cpq), check_cand, st, nullptr, int64_t(0),
+            wait_limit_ns());
         timer_end(K_POOL_SCORE, s);
     }
     const int cap_t = sel_cap(8 * int64_t(C));
@@ -1658,7 +1674,8 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         int64_t chunks = ceil_div<int64_t>(8 * int64_t(sm_count()), groups);
         chunks = chunks < 1 ? 1 : (chunks > tiles ? tiles : chunks);
         timer_begin(K_SCAN, s);
-        launch(scan_mq_kernel, dim3(unsigned(chunks), unsigned(groups)), kMqThreads, sizeof(MqSmem), s, 1, q_codes,
+        launch(k_scales == nullptr ? scan_mq_kernel<true> : scan_mq_kernel<false>,
+               dim3(unsigned(chunks), unsigned(groups)), kMqThreads, sizeof(MqSmem), s, 1, q_codes,
                q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, n_q, blockmax, L.nb_stride,
                st, wait_limit_ns());
         timer_end(K_SCAN, s);
@@ -1666,7 +1683,8 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
         const int64_t cpq = tc_ctas_per_query(n_q, ceil_div<int64_t>(max_visible, kTile));
         const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
         timer_begin(K_SCAN, s);
-        launch(score_tc_kernel<false>, grid, kTcThreads, sizeof(TcScanSmem), s, 1,
+        launch(k_scales == nullptr ? score_tc_kernel<false, true> : score_tc_kernel<false, false>, grid,
+            kTcThreads, sizeof(TcScanSmem), s, 1,
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0,
             (n_q <= kScanMaxQ && n_q <= sm_count()) ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st,
             L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride, wait_limit_ns());

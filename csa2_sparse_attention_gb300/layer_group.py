@@ -87,14 +87,9 @@ class LayerGroup:
         self.kv_codes = torch.zeros((self.n_rows, 256), dtype=u8, device=d)
         self.kv_scales = torch.zeros((self.n_rows, 32), dtype=u8, device=d)
         # indexer K: 576-byte records of 8 rows (codes then scales), or BLOCK8
-        # codes with a separate scale plane.  By default decode caches use the
-        # records (the pool gather reads a block in one copy) and shared
-        # prefill caches the split form: the many-query scan's 128-row MMA
-        # operand then has its 8-row groups on 128-byte boundaries (512 B
-        # apart instead of 576), and that scan, bound by its epilogue and MMA
-        # issue rather than by memory, runs faster on it.
+        # codes with a separate scale plane
         if ik_layout is None:
-            ik_layout = abi.LAYOUT_BLOCK8 if wl.shared_cache else abi.LAYOUT_BLOCK8R
+            ik_layout = abi.LAYOUT_BLOCK8R
         self.ik_layout = ik_layout
         if ik_layout == abi.LAYOUT_BLOCK8R:
             self.ik_codes = torch.zeros((self.n_rows // 8 * 576,), dtype=u8, device=d)
