@@ -20,7 +20,9 @@
 #include "csa2_pipe.cuh"
 #include "csa2_tc.cuh"
 
+#include <climits>
 #include <cooperative_groups.h>
+#include <cuda.h>  // CUtensorMap and the tensor-map encoder's types (the encoder is fetched from the driver at run time)
 
 namespace csa2 {
 
@@ -201,7 +203,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const uint8_t* __restrict__ k_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, int32_t max_visible, const int32_t* __restrict__ cand,
     int64_t cand_stride, int C, float* __restrict__ out, int64_t out_stride, int ctas_per_query,
-    bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride, uint64_t wlim) {
+    bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride, uint64_t wlim,
+    const __grid_constant__ CUtensorMap kmap, bool use_map) {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
     constexpr bool rec = REC;  // indexer K as 576-byte records (k_scales unused)
@@ -315,6 +318,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
                 const bool live = bl >= 0 && bl < nblk_vis && (lane < 16 || !rec);
                 if (lane < 16 && !live && check_cand && (bl < -1 || bl >= nblk_vis))
                     record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_POOL, int32_t(q), bl);
+                if (rec && use_map) {
+                    // four TMA gathers of four records each (lanes 0..3); a
+                    // slot without a valid block re-reads the query's first
+                    // block, whose scores the epilogue discards
+                    const int32_t row = int32_t((ks >> 3) + (live ? bl : 0));
+                    const int g4 = 4 * (lane & 3);
+                    const int32_t r0 = __shfl_sync(0xffffffffu, row, g4), r1 = __shfl_sync(0xffffffffu, row, g4 + 1);
+                    const int32_t r2 = __shfl_sync(0xffffffffu, row, g4 + 2), r3 = __shfl_sync(0xffffffffu, row, g4 + 3);
+                    if (lane == 0) mbar_arrive_expect_tx(&S.full[s], 16 * 576);
+                    __syncwarp();
+                    if (lane < 4) tma_gather4(stage_codes<rec>(S.ring, s) + g4 * 576, &kmap, r0, r1, r2, r3, &S.full[s]);
+                    issued = i + 1;
+                    continue;
+                }
                 const uint32_t bytes = __reduce_add_sync(0xffffffffu, live ? (lane < 16 ? (rec ? 576u : 512u) : 64u) : 0u);
                 if (lane == 0) mbar_arrive_expect_tx(&S.full[s], bytes);  // 0 bytes: the phase completes at once
                 __syncwarp();
@@ -1573,6 +1590,40 @@ static csa2_status prepare_select_kernels() {
     return CSA2_OK;
 }
 
+// The driver's tensor-map encoder, fetched once (null when unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult res = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &res) !=
+                cudaSuccess ||
+            res != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return EncodeTiledFn(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A tensor map over indexer-K records viewed as [n_rows / 8][144] 32-bit
+// words with one-row boxes, for the pool gather's four-record TMA gathers.
+// False when none can be made; the gather then copies record by record.
+static bool records_map(CUtensorMap* m, const uint8_t* k_codes, int64_t n_rows) {
+    const int64_t nb = n_rows / 8;
+    const EncodeTiledFn enc = encode_tiled();
+    if (enc == nullptr || nb <= 0 || nb > INT32_MAX) return false;
+    const cuuint64_t dim[2] = {144, cuuint64_t(nb)};
+    const cuuint64_t stride[1] = {576};
+    const cuuint32_t box[2] = {144, 1}, step[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(k_codes), dim, stride, box, step,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // CTAs per query for a tensor-core scorer launch: two resident CTAs per SM
 // over the whole batch, at most one per tile.
 static int64_t tc_ctas_per_query(int64_t n_q, int64_t tiles_max) {
@@ -1627,11 +1678,13 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
     if (pos_scores == nullptr) {
         const int64_t cpq = tc_ctas_per_query(n_q, (C + 15) / 16);
         const dim3 grid(static_cast<unsigned>(cpq), static_cast<unsigned>(n_q));
+        CUtensorMap kmap = {};
+        const bool use_map = k_scales == nullptr && records_map(&kmap, k_codes, n_rows);
         timer_begin(K_POOL_SCORE, s);
         launch(k_scales == nullptr ? score_tc_kernel<true, true> : score_tc_kernel<true, false>, grid, kTcThreads,
             sizeof(TcScanSmem), s, 1, q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible,
             max_visible, cand, cand_stride, C, scores, score_stride, int(cpq), check_cand, st, nullptr, int64_t(0),
-            wait_limit_ns());
+            wait_limit_ns(), kmap, use_map);
         timer_end(K_POOL_SCORE, s);
     }
     const int cap_t = sel_cap(8 * int64_t(C));
@@ -1687,7 +1740,8 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
             kTcThreads, sizeof(TcScanSmem), s, 1,
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0,
             (n_q <= kScanMaxQ && n_q <= sm_count()) ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st,
-            L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride, wait_limit_ns());
+            L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride, wait_limit_ns(),
+            CUtensorMap{}, false);
         timer_end(K_SCAN, s);
     }
     launch_select_blocks(blockmax, L.nb_stride, n_q, kv_start, n_visible, max_visible, n_rows, pool_blocks,

@@ -79,4 +79,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// One TMA gather: four one-row boxes of a 2-D tensor map (rows r0..r3, from
+// column 0) into consecutive box-sized slots at dst, completing their bytes
+// on the barrier.  dst 128-byte aligned; the map lives in kernel parameter
+// space (__grid_constant__).
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 }  // namespace csa2
