@@ -42,6 +42,8 @@ EXPORTS = {
     "csa2_quantize_append": (_int, [_p, _i64, _int, _int, _int, _p, _p, _i64, _p, _i64, _p, _p, _p, _sz, _p]),
     "csa2_index_full": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _int, _int, _p, _p, _p, _sz, _p]),
     "csa2_index_reindex": (_int, [_p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p, _p, _sz, _p]),
+    "csa2_index_full_bf16": (_int, [_p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _int, _int, _p, _p, _p, _sz, _p]),
+    "csa2_index_reindex_bf16": (_int, [_p, _p, _i64, _p, _p, _i64, _p, _p, _i32, _p, _int, _int, _p, _p, _sz, _p]),
     "csa2_sparse_attn": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _p, _int, ctypes.c_float,
                                 _p, _int, _p, _p, _sz, _p]),
     "csa2_sparse_attn_prefill": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _p, _int, _p, _int, ctypes.c_float,
@@ -140,6 +142,22 @@ def csa2_index_reindex(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_
         _ptr(q_codes), _ptr(q_scales), _ptr(w), n_q, _ptr(k_codes), _ptr(k_scales), n_rows,
         _ptr(kv_start), _ptr(n_visible), max_visible, _ptr(pool), pool_blocks, topk, _ptr(out_topk),
         _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def csa2_index_full_bf16(q_bf16, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible,
+                         pool_blocks, topk, out_pool, out_topk, ws, ws_bytes, stream=None):
+    """csa2_index_full with the indexer query as bf16 rows [n_q * 32][128]."""
+    return _check("csa2_index_full_bf16", lib.csa2_index_full_bf16(
+        _ptr(q_bf16), _ptr(w), n_q, _ptr(k_codes), _ptr(k_scales), n_rows, _ptr(kv_start), _ptr(n_visible),
+        max_visible, pool_blocks, topk, _ptr(out_pool), _ptr(out_topk), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def csa2_index_reindex_bf16(q_bf16, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible,
+                            pool, pool_blocks, topk, out_topk, ws, ws_bytes, stream=None):
+    """csa2_index_reindex with the indexer query as bf16 rows [n_q * 32][128]."""
+    return _check("csa2_index_reindex_bf16", lib.csa2_index_reindex_bf16(
+        _ptr(q_bf16), _ptr(w), n_q, _ptr(k_codes), _ptr(k_scales), n_rows, _ptr(kv_start), _ptr(n_visible),
+        max_visible, _ptr(pool), pool_blocks, topk, _ptr(out_topk), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def csa2_index_reindex_noalloc(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible,

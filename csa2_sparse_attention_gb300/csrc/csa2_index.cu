@@ -96,6 +96,7 @@ __device__ __forceinline__ uint8_t* stage_scales(uint8_t* ring, int s, int row) 
 struct TcScanSmem {
     uint8_t ring[kTcStages * kStageBytes];
     uint8_t qcodes[32 * 64];          // the query's 32 heads, BLOCK8 = canonical K-major
+    uint8_t qsc[32 * 8];              // their scales, when the query arrives as bf16
     int32_t cand[kTcMaxCandPerCta];   // this CTA's candidate blocks (pool scoring)
     uint64_t full[kTcStages], empty[kTcStages];
     uint64_t sfa_ready[kTcSf];
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     const int32_t* __restrict__ n_visible, int32_t max_visible, const int32_t* __restrict__ cand,
     int64_t cand_stride, int C, float* __restrict__ out, int64_t out_stride, int ctas_per_query,
     bool check_cand, Status* st, float* __restrict__ pos_scores, int64_t pos_stride, uint64_t wlim,
-    const __grid_constant__ CUtensorMap kmap, bool use_map) {
+    const __grid_constant__ CUtensorMap kmap, bool use_map, const uint16_t* __restrict__ q_bf16) {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     TcScanSmem& S = *reinterpret_cast<TcScanSmem*>(tc_smem_raw);
     constexpr bool rec = REC;  // indexer K as 576-byte records (k_scales unused)
@@ -275,11 +276,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
     // whose MMAs were issued: what a give-up must wait for before TMEM and
     // shared memory are released
     int issued = 0, mma_n = 0;
+    if (q_bf16 != nullptr && warp > 0) {
+        // the query as bf16: warps 1..5 quantize its 32 heads (256 groups of
+        // 16 channels) into the MMA's B operand and its scales, exactly as
+        // the FP4 append does, while warp 0 already streams K tiles
+        for (int grp = int(threadIdx.x) - 32; grp < 256; grp += kTcThreads - 32) {
+            const int h = grp >> 3, g = grp & 7;
+            const uint4* src = reinterpret_cast<const uint4*>(q_bf16 + (q * 32 + h) * 128 + 16 * g);
+            const uint4 a = __ldg(src), b = __ldg(src + 1);
+            const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[2 * j] = bf16_lo(wv[j]);
+                v[2 * j + 1] = bf16_hi(wv[j]);
+            }
+            uint32_t cw[2];
+            S.qsc[h * 8 + g] = uint8_t(quantize_group16(v, cw));
+            *reinterpret_cast<uint2*>(S.qcodes + (h >> 3) * 512 + (g >> 1) * 128 + (h & 7) * 16 + (g & 1) * 8) =
+                make_uint2(cw[0], cw[1]);
+        }
+        fence_async_smem();  // the codes are the MMA's operand
+        asm volatile("bar.sync 1, %0;" ::"n"(kTcThreads - 32) : "memory");
+    }
 
     if (warp == 0) {  // ------------------------------------------ producer
         // the scan copies a tile with two bulk copies from lane 0; the gather
         // spreads a tile's 32 copies (16 blocks x codes, scales) over the lanes
-        if (lane == 0) {
+        if (lane == 0 && q_bf16 == nullptr) {
             mbar_arrive_expect_tx(&S.qbar, 32 * 64);
             bulk_g2s(S.qcodes, q_codes + (q * 32 / 8) * 512, 32 * 64, &S.qbar);
         }
@@ -351,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         }
     } else if (warp == 1) {  // ----------------------------------- MMA issue
         if (lane == 0) {
-            bool ok = mbar_wait(&S.qbar, 0, wlim);
+            bool ok = q_bf16 != nullptr || mbar_wait(&S.qbar, 0, wlim);
             constexpr uint32_t id = idesc_mxf4nvf4(128, 32);
             const uint32_t qa = smem_u32(S.qcodes);
             for (int i = 0; ok && i < ntiles; ++i) {
@@ -382,7 +406,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
 #pragma unroll
         for (int h = 0; h < 32; ++h) wv[h] = __ldg(w + q * 32 + h);
         {  // the query's scales (B), replicated in every quadrant
-            const uint2 qs = __ldg(reinterpret_cast<const uint2*>(q_scales + (q * 32 + lane) * 8));
+            const uint2 qs = q_bf16 != nullptr ? *reinterpret_cast<const uint2*>(S.qsc + lane * 8)
+                                               : __ldg(reinterpret_cast<const uint2*>(q_scales + (q * 32 + lane) * 8));
             tmem_st4(lane_base + kColSfb, qs.x, 0u, 0u, 0u);
             tmem_st4(lane_base + kColSfb + 4, qs.y, 0u, 0u, 0u);
         }
@@ -450,7 +475,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
         // a wait gave up: wait for the copies and MMAs already issued (the
         // last commit covers every earlier MMA) before anything is released
         if (lane == 0 && warp == 0) {
-            mbar_wait(&S.qbar, 0, kDrainNs);
+            if (q_bf16 == nullptr) mbar_wait(&S.qbar, 0, kDrainNs);
             for (int i = issued > kTcStages ? issued - kTcStages : 0; i < issued; ++i)
                 mbar_wait(&S.full[i % kTcStages], (i / kTcStages) & 1, kDrainNs);
         } else if (lane == 0 && warp == 1 && mma_n > 0) {
@@ -1543,16 +1568,19 @@ __global__ void __launch_bounds__(kMqThreads, 1) scan_mq_kernel(
 }
 
 // ------------------------------------------------------------ launches
-static csa2_status check_index_args(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
-                                    int64_t n_q, const uint8_t* k_codes, const uint8_t* k_scales,
+// q_bf16 non-null: the query arrives as bf16 rows (q_codes, q_scales unused)
+static csa2_status check_index_args(const uint8_t* q_codes, const uint8_t* q_scales, const void* q_bf16,
+                                    const float* w, int64_t n_q, const uint8_t* k_codes, const uint8_t* k_scales,
                                     int64_t n_rows, const int64_t* kv_start,
                                     const int32_t* n_visible, int32_t max_visible,
                                     int pool_blocks, int topk) {
     if (n_q < 0 || n_rows < 0 || max_visible < 0) return CSA2_ERR_INVALID_ARG;
     // k_scales NULL: k_codes holds 576-byte records (CSA2_LAYOUT_BLOCK8R)
-    if (!q_codes || !q_scales || !w || !k_codes || !kv_start || !n_visible) return CSA2_ERR_INVALID_ARG;
-    if (!aligned16(q_codes) || !aligned16(k_codes) || (k_scales && !aligned16(k_scales)) || !aligned16(q_scales))
+    if (!w || !k_codes || !kv_start || !n_visible) return CSA2_ERR_INVALID_ARG;
+    if (q_bf16 != nullptr ? !aligned16(q_bf16)
+                          : (!q_codes || !q_scales || !aligned16(q_codes) || !aligned16(q_scales)))
         return CSA2_ERR_INVALID_ARG;
+    if (!aligned16(k_codes) || (k_scales && !aligned16(k_scales))) return CSA2_ERR_INVALID_ARG;
     if (n_rows % 8) return CSA2_ERR_UNSUPPORTED;
     if (pool_blocks < 1 || pool_blocks > kMaxPoolBlocks || topk < 1 || topk > kMaxTopk)
         return CSA2_ERR_UNSUPPORTED;
@@ -1672,7 +1700,8 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
                              const int64_t* kv_start, const int32_t* n_visible, int32_t max_visible,
                              const int32_t* cand, int64_t cand_stride, int C, int topk, int32_t* out_topk,
                              float* scores, int64_t score_stride, bool check_cand, Status* st, cudaStream_t s,
-                             const float* pos_scores = nullptr, int64_t pos_stride = 0) {
+                             const float* pos_scores = nullptr, int64_t pos_stride = 0,
+                             const uint16_t* q_bf16 = nullptr) {
     // with the scan's per-position scores at hand (pos_scores), the candidates
     // are not scored again: the selection reads their scores from there
     if (pos_scores == nullptr) {
@@ -1684,7 +1713,7 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
         launch(k_scales == nullptr ? score_tc_kernel<true, true> : score_tc_kernel<true, false>, grid, kTcThreads,
             sizeof(TcScanSmem), s, 1, q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible,
             max_visible, cand, cand_stride, C, scores, score_stride, int(cpq), check_cand, st, nullptr, int64_t(0),
-            wait_limit_ns(), kmap, use_map);
+            wait_limit_ns(), kmap, use_map, q_bf16);
         timer_end(K_POOL_SCORE, s);
     }
     const int cap_t = sel_cap(8 * int64_t(C));
@@ -1699,14 +1728,15 @@ static void launch_pool_topk(const uint8_t* q_codes, const uint8_t* q_scales, co
 
 using namespace csa2;
 
-extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
-                                       int64_t n_q, const uint8_t* k_codes, const uint8_t* k_scales,
-                                       int64_t n_rows, const int64_t* kv_start,
-                                       const int32_t* n_visible, int32_t max_visible,
-                                       int pool_blocks, int topk, int32_t* out_pool,
-                                       int32_t* out_topk, void* ws, size_t ws_bytes,
-                                       csa2_stream_t stream) {
-    csa2_status e = check_index_args(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start,
+// csa2_index_full, with the query as FP4 (q_codes, q_scales) or as bf16
+// rows (q_bf16): the decode scorers quantize a bf16 query in their
+// prologue; the many-query scan reads it quantized into the workspace.
+static csa2_status index_full(const uint8_t* q_codes, const uint8_t* q_scales, const uint16_t* q_bf16,
+                              const float* w, int64_t n_q, const uint8_t* k_codes, const uint8_t* k_scales,
+                              int64_t n_rows, const int64_t* kv_start, const int32_t* n_visible,
+                              int32_t max_visible, int pool_blocks, int topk, int32_t* out_pool, int32_t* out_topk,
+                              void* ws, size_t ws_bytes, csa2_stream_t stream) {
+    csa2_status e = check_index_args(q_codes, q_scales, q_bf16, w, n_q, k_codes, k_scales, n_rows, kv_start,
                                      n_visible, max_visible, pool_blocks, topk);
     if (e != CSA2_OK) return e;
     if (!out_pool || !out_topk) return CSA2_ERR_INVALID_ARG;
@@ -1720,6 +1750,18 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
     float* blockmax = reinterpret_cast<float*>(base + L.blockmax);
     float* scores = reinterpret_cast<float*>(base + L.scores);
     const int C = pool_blocks > topk ? pool_blocks : topk;
+    if (q_bf16 != nullptr && n_q >= kMqMinQueries) {
+        // the many-query scan shares each query's FP4 operand across CTAs:
+        // quantize it once into the workspace, then index as from FP4
+        uint8_t* qc = reinterpret_cast<uint8_t*>(base + L.qcodes);
+        uint8_t* qs = reinterpret_cast<uint8_t*>(base + L.qscales);
+        if ((e = csa2_quantize_append(q_bf16, n_q * 32, 128, CSA2_FMT_FP4, CSA2_LAYOUT_BLOCK8, nullptr, nullptr, 0,
+                                      nullptr, n_q * 32, qc, qs, ws, ws_bytes, stream)) != CSA2_OK)
+            return e;
+        q_codes = qc;
+        q_scales = qs;
+        q_bf16 = nullptr;
+    }
     if (max_visible > 0 && n_q >= kMqMinQueries) {
         // many queries: groups of 4 share each K tile; about 8 waves of one CTA per SM
         const int64_t groups = ceil_div<int64_t>(n_q, kMqQ);
@@ -1741,7 +1783,7 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
             q_codes, q_scales, w, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, nullptr, 0,
             (n_q <= kScanMaxQ && n_q <= sm_count()) ? int(n_q) : 0, blockmax, L.nb_stride, int(cpq), false, st,
             L.pos_stride ? reinterpret_cast<float*>(base + L.pos) : nullptr, L.pos_stride, wait_limit_ns(),
-            CUtensorMap{}, false);
+            CUtensorMap{}, false, q_bf16);
         timer_end(K_SCAN, s);
     }
     launch_select_blocks(blockmax, L.nb_stride, n_q, kv_start, n_visible, max_visible, n_rows, pool_blocks,
@@ -1759,18 +1801,41 @@ extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_
     launch_pool_topk(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, cand,
                      cand_stride, C, topk, out_topk, scores, L.score_stride, false, st, s,
                      L.pos_stride && max_visible > 0 ? reinterpret_cast<const float*>(base + L.pos) : nullptr,
-                     L.pos_stride);
+                     L.pos_stride, q_bf16);
     return launch_status();
 }
 
-extern "C" csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t* q_scales,
-                                          const float* w, int64_t n_q, const uint8_t* k_codes,
-                                          const uint8_t* k_scales, int64_t n_rows,
-                                          const int64_t* kv_start, const int32_t* n_visible,
-                                          int32_t max_visible, const int32_t* pool, int pool_blocks,
-                                          int topk, int32_t* out_topk, void* ws, size_t ws_bytes,
-                                          csa2_stream_t stream) {
-    csa2_status e = check_index_args(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start,
+extern "C" csa2_status csa2_index_full(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                                       int64_t n_q, const uint8_t* k_codes, const uint8_t* k_scales,
+                                       int64_t n_rows, const int64_t* kv_start,
+                                       const int32_t* n_visible, int32_t max_visible,
+                                       int pool_blocks, int topk, int32_t* out_pool,
+                                       int32_t* out_topk, void* ws, size_t ws_bytes,
+                                       csa2_stream_t stream) {
+    return index_full(q_codes, q_scales, nullptr, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible,
+                      max_visible, pool_blocks, topk, out_pool, out_topk, ws, ws_bytes, stream);
+}
+
+extern "C" csa2_status csa2_index_full_bf16(const void* q_bf16, const float* w, int64_t n_q,
+                                            const uint8_t* k_codes, const uint8_t* k_scales, int64_t n_rows,
+                                            const int64_t* kv_start, const int32_t* n_visible,
+                                            int32_t max_visible, int pool_blocks, int topk, int32_t* out_pool,
+                                            int32_t* out_topk, void* ws, size_t ws_bytes,
+                                            csa2_stream_t stream) {
+    if (!q_bf16) return CSA2_ERR_INVALID_ARG;
+    return index_full(nullptr, nullptr, static_cast<const uint16_t*>(q_bf16), w, n_q, k_codes, k_scales, n_rows,
+                      kv_start, n_visible, max_visible, pool_blocks, topk, out_pool, out_topk, ws, ws_bytes,
+                      stream);
+}
+
+// csa2_index_reindex with the query as FP4 or (q_bf16) as bf16 rows,
+// quantized by the pool scorer's prologue
+static csa2_status index_reindex(const uint8_t* q_codes, const uint8_t* q_scales, const uint16_t* q_bf16,
+                                 const float* w, int64_t n_q, const uint8_t* k_codes, const uint8_t* k_scales,
+                                 int64_t n_rows, const int64_t* kv_start, const int32_t* n_visible,
+                                 int32_t max_visible, const int32_t* pool, int pool_blocks, int topk,
+                                 int32_t* out_topk, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+    csa2_status e = check_index_args(q_codes, q_scales, q_bf16, w, n_q, k_codes, k_scales, n_rows, kv_start,
                                      n_visible, max_visible, pool_blocks, topk);
     if (e != CSA2_OK) return e;
     if (!pool || !out_topk) return CSA2_ERR_INVALID_ARG;
@@ -1783,8 +1848,31 @@ extern "C" csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t*
     Status* st = reinterpret_cast<Status*>(base);
     float* scores = reinterpret_cast<float*>(base + L.scores);
     launch_pool_topk(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible, max_visible, pool,
-                     pool_blocks, pool_blocks, topk, out_topk, scores, L.score_stride, true, st, s);
+                     pool_blocks, pool_blocks, topk, out_topk, scores, L.score_stride, true, st, s, nullptr, 0,
+                     q_bf16);
     return launch_status();
+}
+
+extern "C" csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t* q_scales,
+                                          const float* w, int64_t n_q, const uint8_t* k_codes,
+                                          const uint8_t* k_scales, int64_t n_rows,
+                                          const int64_t* kv_start, const int32_t* n_visible,
+                                          int32_t max_visible, const int32_t* pool, int pool_blocks,
+                                          int topk, int32_t* out_topk, void* ws, size_t ws_bytes,
+                                          csa2_stream_t stream) {
+    return index_reindex(q_codes, q_scales, nullptr, w, n_q, k_codes, k_scales, n_rows, kv_start, n_visible,
+                         max_visible, pool, pool_blocks, topk, out_topk, ws, ws_bytes, stream);
+}
+
+extern "C" csa2_status csa2_index_reindex_bf16(const void* q_bf16, const float* w, int64_t n_q,
+                                               const uint8_t* k_codes, const uint8_t* k_scales, int64_t n_rows,
+                                               const int64_t* kv_start, const int32_t* n_visible,
+                                               int32_t max_visible, const int32_t* pool, int pool_blocks, int topk,
+                                               int32_t* out_topk, void* ws, size_t ws_bytes,
+                                               csa2_stream_t stream) {
+    if (!q_bf16) return CSA2_ERR_INVALID_ARG;
+    return index_reindex(nullptr, nullptr, static_cast<const uint16_t*>(q_bf16), w, n_q, k_codes, k_scales, n_rows,
+                         kv_start, n_visible, max_visible, pool, pool_blocks, topk, out_topk, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------ no-allocation variant
@@ -1806,7 +1894,7 @@ extern "C" csa2_status csa2_index_reindex_noalloc(const uint8_t* q_codes, const 
                                                   int32_t max_visible, const int32_t* pool,
                                                   int pool_blocks, int topk, int32_t* out_topk,
                                                   int32_t* status, csa2_stream_t stream) {
-    csa2_status e = check_index_args(q_codes, q_scales, w, n_q, k_codes, k_scales, n_rows, kv_start,
+    csa2_status e = check_index_args(q_codes, q_scales, nullptr, w, n_q, k_codes, k_scales, n_rows, kv_start,
                                      n_visible, max_visible, pool_blocks, topk);
     if (e != CSA2_OK) return e;
     if (!pool || !out_topk) return CSA2_ERR_INVALID_ARG;

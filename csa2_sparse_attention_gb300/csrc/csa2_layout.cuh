@@ -25,7 +25,7 @@ constexpr int64_t kMqMinQueries = 256;
 constexpr int64_t kPosScoreMaxCand = 2048;
 
 struct IndexFullWs {
-    size_t blockmax, cand, scores, pos, total;
+    size_t blockmax, cand, scores, pos, qcodes, qscales, total;
     int64_t nb_stride, cand_stride, score_stride, pos_stride;  // pos_stride 0: no per-position scores
 };
 __host__ __device__ inline IndexFullWs index_full_ws(int64_t n_q, int64_t max_visible, int P, int K) {
@@ -44,6 +44,13 @@ __host__ __device__ inline IndexFullWs index_full_ws(int64_t n_q, int64_t max_vi
     if (w.pos_stride == 0) off = align256(off + size_t(n_q) * size_t(w.score_stride) * 4);
     w.pos = off;
     off = align256(off + size_t(n_q) * size_t(w.pos_stride) * 4);
+    // csa2_index_full_bf16 with many queries: the query quantized to FP4
+    // (BLOCK8 codes, scales) for the many-query scan
+    const size_t qrows = n_q >= kMqMinQueries ? size_t(n_q) * 32 : 0;
+    w.qcodes = off;
+    off = align256(off + qrows * 64);
+    w.qscales = off;
+    off = align256(off + qrows * 8);
     w.total = off;
     return w;
 }

@@ -61,8 +61,12 @@ class LayerGroup:
     """Caches, per-layer inputs/outputs and workspaces of one workload."""
 
     def __init__(self, wl: W.Workload, device="cuda", sm_scale=1.0 / math.sqrt(512.0),
-                 rope_theta=10000.0, out_dtype=torch.float32, ik_layout=None):
+                 rope_theta=10000.0, out_dtype=torch.float32, ik_layout=None, fused_q=True):
         self.wl = wl
+        # fused_q: the index calls take the bf16 indexer query and quantize it
+        # themselves (csa2_index_*_bf16); else a separate FP4 append per layer
+        # fills iq_codes / iq_scales first
+        self.fused_q = fused_q
         self.dev = torch.device(device)
         self.B = wl.batch
         self.layers = wl.layers
@@ -247,6 +251,17 @@ class LayerGroup:
         """The index part of a layer (Full / Reindex; Reuse makes no call)."""
         mode = self.layers[li]
         B = self.B
+        if self.fused_q:
+            if mode == W.FULL:
+                abi.csa2_index_full_bf16(self.iq_bf16[li], self.iw[li], B, self.ik_codes, self.ik_scales, self.n_rows,
+                                         self.kv_start, self.n_visible, self.max_visible, self.P, self.K,
+                                         self.pools[li], self.topk[li], self.ws_full, self.ws_full.numel(), s)
+            elif mode == W.REINDEX:
+                abi.csa2_index_reindex_bf16(self.iq_bf16[li], self.iw[li], B, self.ik_codes, self.ik_scales,
+                                            self.n_rows, self.kv_start, self.n_visible, self.max_visible,
+                                            self.pools[self.group_full(li)], self.P, self.K, self.topk[li],
+                                            self.ws_re, self.ws_re.numel(), s)
+            return
         if mode in (W.FULL, W.REINDEX):
             abi.csa2_quantize_append(self.iq_bf16[li], B * 32, 128, abi.FMT_FP4, abi.LAYOUT_BLOCK8, None, None,
                                      0, None, B * 32, self.iq_codes[li], self.iq_scales[li], self.ws_app,

@@ -10,6 +10,8 @@
  *                              the top-k positions.
  *   3. csa2_index_reindex    - Reindex layer: re-score only the pool's
  *                              positions with this layer's own indexer query.
+ *      (csa2_index_full_bf16 / csa2_index_reindex_bf16 take the indexer
+ *      query as bf16 and quantize it themselves, saving its FP4 append.)
  *      (Reuse layers make no call: they pass the previous top-k buffer again.)
  *   4. csa2_sparse_attn      - 64-head attention over the selected FP4 latents
  *                              plus the FP8 sliding window, one merged softmax.
@@ -203,6 +205,30 @@ csa2_status csa2_index_reindex(const uint8_t* q_codes, const uint8_t* q_scales, 
                                int64_t n_rows, const int64_t* kv_start, const int32_t* n_visible,
                                int32_t max_visible, const int32_t* pool, int pool_blocks, int topk,
                                int32_t* out_topk, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/*
+ * csa2_index_full and csa2_index_reindex with the indexer query given as
+ * bf16 rows, q_bf16 [n_q*32][128] (row t*32+h is head h of query t, 16-byte
+ * aligned), instead of FP4 codes and scales.  The query is quantized to FP4
+ * (E2M1, one E4M3 scale per 16 channels; [T1] 层级化稀疏索引器, [T3] 第二刀:
+ * the indexer runs in FP4) inside the call, exactly as csa2_quantize_append
+ * with CSA2_FMT_FP4 would, so the results are those of the FP4 calls on that
+ * quantization.  Decode batches (fewer than 256 queries) and every Reindex
+ * call quantize it in the scoring kernels' prologue, which saves the
+ * separate quantization launch; a many-query Full call quantizes it into
+ * its workspace first (the workspace size is the same as the FP4 call's).
+ * Other arguments, results and errors as in the FP4 calls.
+ */
+csa2_status csa2_index_full_bf16(const void* q_bf16, const float* w, int64_t n_q, const uint8_t* k_codes,
+                                 const uint8_t* k_scales, int64_t n_rows, const int64_t* kv_start,
+                                 const int32_t* n_visible, int32_t max_visible, int pool_blocks, int topk,
+                                 int32_t* out_pool, int32_t* out_topk, void* ws, size_t ws_bytes,
+                                 csa2_stream_t stream);
+csa2_status csa2_index_reindex_bf16(const void* q_bf16, const float* w, int64_t n_q, const uint8_t* k_codes,
+                                    const uint8_t* k_scales, int64_t n_rows, const int64_t* kv_start,
+                                    const int32_t* n_visible, int32_t max_visible, const int32_t* pool,
+                                    int pool_blocks, int topk, int32_t* out_topk, void* ws, size_t ws_bytes,
+                                    csa2_stream_t stream);
 
 /*
  * csa2_index_reindex without a workspace, for callers that cannot allocate

@@ -89,6 +89,19 @@ def test_host_argument_errors_return_before_launch(abi):
     st = A.lib.csa2_index_full(fake, fake, fake, 1, fake, fake, 16, fake, fake, 100, 2048, 512,
                                fake, fake, fake, 64, None)
     assert st == A.ERR_WORKSPACE
+    # the bf16-query forms: the query pointer is required and 16-byte aligned
+    st = A.lib.csa2_index_full_bf16(None, fake, 1, fake, fake, 16, fake, fake, 100, 2048, 512,
+                                    fake, fake, fake, 1 << 30, None)
+    assert st == A.ERR_INVALID_ARG
+    st = A.lib.csa2_index_full_bf16(fake + 2, fake, 1, fake, fake, 16, fake, fake, 100, 2048, 512,
+                                    fake, fake, fake, 1 << 30, None)
+    assert st == A.ERR_INVALID_ARG
+    st = A.lib.csa2_index_reindex_bf16(None, fake, 1, fake, fake, 16, fake, fake, 100, fake, 2048, 512,
+                                       fake, fake, 1 << 30, None)
+    assert st == A.ERR_INVALID_ARG
+    st = A.lib.csa2_index_reindex_bf16(fake, fake, 1, fake, fake, 12, fake, fake, 100, fake, 2048, 512,
+                                       fake, fake, 1 << 30, None)
+    assert st == A.ERR_UNSUPPORTED  # n_rows not a multiple of 8
     st = A.lib.csa2_sparse_attn(fake, 1, fake, fake, 16, fake, fake, fake, 512, fake, None, 129, 0.04,
                                 fake, A.OUT_F32, None, fake, 1 << 30, None)
     assert st == A.ERR_INVALID_ARG  # window above 128
@@ -115,6 +128,10 @@ def test_empty_batches_return_ok_and_launch_nothing(abi):
                                  fake, fake, fake, 1 << 30, None) == A.OK
     assert A.lib.csa2_index_reindex(fake, fake, fake, 0, fake, fake, 16, fake, fake, 100, fake, 2048, 512,
                                     fake, fake, 1 << 30, None) == A.OK
+    assert A.lib.csa2_index_full_bf16(fake, fake, 0, fake, fake, 16, fake, fake, 100, 2048, 512,
+                                      fake, fake, fake, 1 << 30, None) == A.OK
+    assert A.lib.csa2_index_reindex_bf16(fake, fake, 0, fake, fake, 16, fake, fake, 100, fake, 2048, 512,
+                                         fake, fake, 1 << 30, None) == A.OK
     assert A.lib.csa2_sparse_attn(fake, 0, fake, fake, 16, fake, fake, fake, 512, fake, None, 128, 0.04,
                                   fake, A.OUT_F32, None, fake, 1 << 30, None) == A.OK
     assert A.csa2_launch_count() == c0

@@ -19,7 +19,7 @@ def test_noalloc_reindex_matches_reindex_on_two_calls():
     from csa2_sparse_attention_gb300.layer_group import LayerGroup
     wl = W.small_variant(W.group_128k(), [20000, 8191, 1000, 333, 17, 5], name="noalloc",
                          layers=("F", "X"), pool_blocks=256, topk=512, hot_blocks=4)
-    g = LayerGroup(wl)
+    g = LayerGroup(wl, fused_q=False)  # the step quantizes the indexer queries into iq_codes / iq_scales
     g.fill()
     g.step()
     torch.cuda.synchronize()
@@ -30,6 +30,8 @@ def test_noalloc_reindex_matches_reindex_on_two_calls():
     ws = torch.zeros(abi.csa2_workspace_bytes(abi.OP_INDEX_REINDEX, g.B, g.max_visible, g.P, g.K),
                      dtype=torch.uint8, device="cuda")
     abi.csa2_index_reindex(*args, ref, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert torch.equal(ref, g.topk[li])
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     for _ in range(2):
         out = torch.full((g.B, g.K), -7, dtype=torch.int32, device="cuda")
