@@ -64,10 +64,12 @@ constexpr int kTile = 128;  // positions per tensor-core tile (16 blocks of 8)
 // 16 channels, so the FP4 codes go from shared memory to the tensor core
 // without dequantization.  Warp 0 streams tiles (contiguous blocks for the
 // scan, the candidate blocks for the pool) into a ring of shared-memory
-// stages with bulk copies; warp 1 issues the MMAs; warps 2..5 copy each
-// tile's scales into TMEM and reduce the 32 head scores of every position:
-// the block maxima (scan) or per-position scores (pool).
-constexpr int kTcThreads = 192;
+// stages with bulk copies (the pool's records four at a time with TMA
+// gathers); warp 1 issues the MMAs; warps 2..9, two groups of four taking
+// alternate tiles, copy each tile's scales into TMEM and reduce the 32 head
+// scores of every position: the block maxima (scan) or per-position scores
+// (pool).  One group alone could not keep up with the scan's tile rate.
+constexpr int kTcThreads = 320;     // producer, MMA, two epilogue groups of 4 warps
 constexpr int kTcStages = 8;
 constexpr int kTcAcc = 4;            // accumulator stages (32 TMEM columns each)
 constexpr int kTcSf = 4;             // scale-factor slots (8 columns each)
@@ -198,7 +200,7 @@ __device__ bool scan_map(const int64_t* kv_start, const int32_t* n_visible, int3
 }
 
 template <bool GATHER, bool REC>
-__global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
+__global__ void __launch_bounds__(kTcThreads, 2) score_tc_kernel(
     const uint8_t* __restrict__ q_codes, const uint8_t* __restrict__ q_scales,
     const float* __restrict__ w, const uint8_t* __restrict__ k_codes,
     const uint8_t* __restrict__ k_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
@@ -399,13 +401,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
             }
         }
     } else {  // --------------------------------------------------- epilogue
+        // two groups of 4 warps (one per TMEM lane quadrant) take alternate
+        // tiles: group eg reads the accumulators of tiles eg, eg + 2, ...
+        // and stages those tiles' scales
+        const int eg = (warp - 2) >> 2;         // epilogue group
         const int quad = warp & 3;              // TMEM lane quadrant of this warp
         const int row = 32 * quad + lane;       // position within a tile
         const uint32_t lane_base = tmem + (uint32_t(32 * quad) << 16);
         float wv[32];
 #pragma unroll
         for (int h = 0; h < 32; ++h) wv[h] = __ldg(w + q * 32 + h);
-        {  // the query's scales (B), replicated in every quadrant
+        if (eg == 0) {  // the query's scales (B), replicated in every quadrant
             const uint2 qs = q_bf16 != nullptr ? *reinterpret_cast<const uint2*>(S.qsc + lane * 8)
                                                : __ldg(reinterpret_cast<const uint2*>(q_scales + (q * 32 + lane) * 8));
             tmem_st4(lane_base + kColSfb, qs.x, 0u, 0u, 0u);
@@ -426,17 +432,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(
             return true;
         };
         bool ok = true;
-        for (int i = 0; ok && i < kTcSfLead && i < ntiles; ++i) ok = stage_sf(i);
-        for (int i = 0; ok && i < ntiles; ++i) {
-            // tile i + lead reuses the slot of tile i + lead - kTcSf, whose MMA
-            // finished before tile i - 1's accumulator was read
-            if (i + kTcSfLead < ntiles) ok = stage_sf(i + kTcSfLead);
+        // the four scale slots start free: tiles eg and eg + 2
+        for (int i = eg; ok && i < kTcSf && i < ntiles; i += 2) ok = stage_sf(i);
+        for (int i = eg; ok && i < ntiles; i += 2) {
             const int a = i % kTcAcc;
-            if (!ok || !mbar_wait(&S.acc_full[a], (i / kTcAcc) & 1, wlim)) {
+            if (!mbar_wait(&S.acc_full[a], (i / kTcAcc) & 1, wlim)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // tile i's MMA is done, so the slot of tile i + kTcSf is free
+            if (i + kTcSf < ntiles && !stage_sf(i + kTcSf)) {
+                ok = false;
+                break;
+            }
             uint32_t r[32];
             tmem_ld32(lane_base + kColAcc + 32 * a, r);
             tmem_ld_wait();
