@@ -7,6 +7,8 @@ does, so a layer group stepped with them must give the same bytes as one
 that quantizes each query with its own append launch first: pools, top-k,
 attention outputs and log-sum-exps, bit for bit.
 """
+from dataclasses import replace
+
 import pytest
 import torch
 
@@ -29,6 +31,9 @@ def _cases():
         ("decode-split", W.small_variant(W.group_128k(), (40000, 9001, 20000), name="q16s", layers=("F", "X", "R", "X"),
                                          hot_blocks=8), "split"),
         ("many-query", W.many_query(queries=288, entries=20000, m=1), None),  # >= 256 queries: quantized into ws
+        # a Reindex layer over many queries quantizes in the pool scorer's prologue
+        ("many-query-FXR", replace(W.many_query(queries=288, entries=20000, m=1), name="q16mq", layers=("F", "X", "R")),
+         None),
     ]
 
 
