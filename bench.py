@@ -635,7 +635,7 @@ NCU_NAMES = (("score_tc_kernel<false", "scan_blockmax"), ("score_tc_kernel<true"
              ("score_tc_kernel<0", "scan_blockmax"), ("score_tc_kernel<1", "pool_score"),
              ("select_blocks_kernel", "select_blocks"), ("select_blocks_cluster_kernel", "select_blocks"),
              ("select_topk_kernel", "select_topk"),
-             ("attn_tc_kernel", "attn_split"), ("attn_merge_kernel", "attn_merge"),
+             ("attn_tc_kernel", "attn_split"), ("attn_query_kernel", "attn_split"), ("attn_merge_kernel", "attn_merge"),
              ("quantize_fp4_kernel", "quantize_fp4"), ("quantize_fp8_kernel", "quantize_fp8"))
 
 

@@ -620,6 +620,390 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     if (lse && lane == 0) lse[q * kH + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
+// One CTA per query, for batches of many queries (prefill chunks): the
+// query's entries in 128-entry chunks, one after another, with an online
+// softmax, so no partial outputs and no merge.  Chunk c holds sequence
+// entries [128 c, 128 c + 128) (top-k entries, then window entries).  S^T of
+// a chunk goes to TMEM columns 256..319; O^T accumulates over the chunks in
+// columns 0..255 (4 blocks of 128 dims x 64 heads: P's f16 hi and lo parts
+// are two MMAs into the same columns, as the 512 columns cannot also hold
+// them side by side), and is rescaled in TMEM whenever a head's running
+// maximum rises.  The next chunk's index and rows are loaded while the
+// current chunk's MMAs and softmax run.
+constexpr uint32_t kQColO = 0, kQColS = 256, kQCols = 512;
+// Batches of at least this many queries take attn_query_kernel: one wave of
+// (split, query) CTAs no longer holds them, and one CTA per query avoids the
+// fp32 partials and their merge.
+constexpr int64_t kAttnQueryMin = 128;
+struct AttnQSmem {
+    uint8_t q[64 * 1024];             // Q f16 (B of S^T), for every chunk
+    uint8_t c[kTcE * 1024];           // C of the current chunk
+    uint8_t p[32 * 1024];             // P^T hi/lo of the current chunk
+    float red[4][kH];                 // per lane quadrant, per head
+    float m[kH], l[kH], alpha[kH];    // running max and sum, this chunk's rescale factor
+    int ok[kTcE];                     // entry valid
+    uint32_t qmax[kAttnThreads / 32];
+    uint64_t bar;                     // MMA completion (per chunk: phase 0 S, phase 1 O)
+    uint32_t tmem;
+};
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_query_kernel(
+    const uint16_t* __restrict__ qg, const uint8_t* __restrict__ kv_codes,
+    const uint8_t* __restrict__ kv_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
+    const int32_t* __restrict__ n_visible, const int32_t* __restrict__ topk, int k,
+    uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, bool win_shared, float sm_scale,
+    void* __restrict__ out, bool out_f32, float* __restrict__ out_lse, Status* st, uint64_t wlim) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    AttnQSmem& S = *reinterpret_cast<AttnQSmem*>(smem_raw);
+    const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
+    const int64_t q = blockIdx.x;
+
+    if (tid == 0) {
+        mbar_init(&S.bar, 1);
+        mbar_init_fence();
+    }
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t ks = kv_start[q];
+    const int32_t nv = n_visible[q];
+    const int ent = tid & (kTcE - 1), qa = tid >> 7;  // entry of a chunk; channel quarters qa, qa + 2
+    const int32_t pre0 = ent < k ? topk[q * k + ent] : -1;
+    if (warp == 0) tmem_alloc(&S.tmem, kQCols);
+    auto q_chunk = [&](int j) {  // as in attn_tc_kernel
+        const int g = 16 * warp + j;
+        return (8 * (g >> 4) + (lane & 7)) * 64 + 4 * (g & 15) + (lane >> 3);
+    };
+    uint4 qv[16];
+    {
+        const uint4* qsrc = reinterpret_cast<const uint4*>(qg + q * (kH * kD));
+#pragma unroll
+        for (int j = 0; j < 16; ++j) qv[j] = __ldg(qsrc + q_chunk(j));
+    }
+    int32_t n = 0;
+    if (ks < 0) {
+        if (tid == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_KV_START, int32_t(q), int32_t(ks));
+    } else if (nv < 0 || ks + nv > n_rows) {
+        if (tid == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_ROWS, int32_t(q), nv);
+    } else {
+        n = nv;
+    }
+    const int nw = n < window ? n : window;
+    const int cur_ge = (swa_new != nullptr && nw > 0) ? k + nw - 1 : -1;  // the current token's entry
+    const int nchunks = (k + window + kTcE - 1) / kTcE;
+
+    // this thread's row of sequence entry ge: kind 0 none (zeros), 1 FP4
+    // latent, 2 FP8 window, 3 the current token
+    int kind = 0;
+    uint4 rv[16];
+    uint2 rs0 = make_uint2(0, 0), rs1 = make_uint2(0, 0);
+    auto load_row = [&](int ge, int32_t p) {
+        kind = 0;
+        if (ge < k) {
+            if (p >= 0 && p < n) {
+                kind = 1;
+                const int64_t row = ks + p;
+                const uint4* src = reinterpret_cast<const uint4*>(kv_codes + row * 256);
+                const uint2* ssrc = reinterpret_cast<const uint2*>(kv_scales + row * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    rv[j] = __ldg(src + qa * 4 + j);
+                    rv[4 + j] = __ldg(src + (qa + 2) * 4 + j);
+                }
+                rs0 = __ldg(ssrc + qa);
+                rs1 = __ldg(ssrc + qa + 2);
+            } else if (p < -1 || p >= n) {
+                if (qa == 0) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_TOPK, int32_t(q), p);
+            }
+        } else if (ge - k < nw) {
+            if (ge == cur_ge) {
+                kind = 3;
+            } else {
+                kind = 2;
+                const int64_t pos = int64_t(n - nw) + (ge - k);
+                const uint4* ring = reinterpret_cast<const uint4*>(
+                    swa + (win_shared ? ks + pos : q * window + pos % window) * kD);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    rv[j] = ring[qa * 8 + j];
+                    rv[8 + j] = ring[(qa + 2) * 8 + j];
+                }
+            }
+        }
+    };
+    load_row(ent, pre0);
+
+    // Q as f16 times 2^-qs (as in attn_tc_kernel)
+    {
+        uint32_t am = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            am = __vmaxu2(am, __vmaxu2(qv[j].x & 0x7FFF7FFFu, qv[j].y & 0x7FFF7FFFu));
+            am = __vmaxu2(am, __vmaxu2(qv[j].z & 0x7FFF7FFFu, qv[j].w & 0x7FFF7FFFu));
+        }
+        am = __reduce_max_sync(0xffffffffu, max(am & 0xFFFFu, am >> 16));
+        if (lane == 0) S.qmax[warp] = am;
+    }
+    if (tid < kH) {
+        S.m[tid] = -INFINITY;
+        S.l[tid] = 0.f;
+    }
+    __syncthreads();  // max |Q| per warp, the running statistics, the barrier
+    int qs = 0;
+    {
+        uint32_t am = 0;
+#pragma unroll
+        for (int w = 0; w < kAttnThreads / 32; ++w) am = max(am, S.qmax[w]);
+        if (am != 0) qs = int(am >> 7) - 127 - 14;
+        qs = qs < -126 ? -126 : (qs > 126 ? 126 : qs);
+        const float qf = __uint_as_float(uint32_t(127 - qs) << 23);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = q_chunk(j);
+            const uint32_t wv[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const __half2 h = __floats2half2_rn(__uint_as_float(wv[m] << 16) * qf,
+                                                    __uint_as_float(wv[m] & 0xFFFF0000u) * qf);
+                o[m] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(S.q + row512(i >> 6, i & 63)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    const float sm_eff = sm_scale * __uint_as_float(uint32_t(127 + qs) << 23);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem;
+    const uint32_t sm_c = smem_addr(S.c), sm_q = smem_addr(S.q), pb = smem_addr(S.p);
+    const int qd = warp & 3, hf = warp >> 2, e = 32 * qd + lane, hl = 32 * hf + lane;
+    float(*red)[kH] = S.red;
+    // ok: every wait so far succeeded.  pend (thread 0): 1 + the parity of a
+    // commit issued but not yet seen complete, else 0
+    bool ok = true;
+    uint32_t pend = 0;
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int ge = c * kTcE + ent;
+        // the next chunk's index, in flight while this chunk is processed
+        const int ge2 = ge + kTcE;
+        const int32_t pre_next = ge2 < k ? topk[q * k + ge2] : -1;
+        if (c > 0) {  // C and P are free once the previous chunk's O MMA is done
+            const bool w = __syncthreads_and(ok && mbar_wait(&S.bar, 1, wlim));
+            if (w) pend = 0;
+            ok = w;
+            tc_fence_after();
+        }
+        if (cur_ge >= c * kTcE && cur_ge < (c + 1) * kTcE) {
+            // two channels per thread: to the ring and into C
+            const int ce = cur_ge - c * kTcE;
+            uint8_t* ring = swa + (q * window + int64_t(n - 1) % window) * kD;
+            const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid);
+            const uint32_t b2 = e4m3x2_rn_sat(bf16_lo(x), bf16_hi(x));
+            reinterpret_cast<uint16_t*>(ring)[tid] = static_cast<uint16_t>(b2);
+            uint32_t h2[2];
+            e4m3x4_to_f16x2(b2, h2);
+            if (ok) *reinterpret_cast<uint32_t*>(S.c + row512(ce, tid >> 2) + (tid & 3) * 4) = h2[0];
+        }
+        if (ok) {  // dequantize this thread's row into C
+            if (kind == 1) {
+                fp4_quarter_to_c(rv, rs0, S.c, ent, qa);
+                fp4_quarter_to_c(rv + 4, rs1, S.c, ent, qa + 2);
+            } else if (kind == 2) {
+                fp8_quarter_to_c(rv, S.c, ent, qa);
+                fp8_quarter_to_c(rv + 8, S.c, ent, qa + 2);
+            } else if (kind == 0) {
+#pragma unroll 1
+                for (int h2 = 0; h2 < 2; ++h2)
+                    for (int cc = (qa + 2 * h2) * 16; cc < (qa + 2 * h2) * 16 + 16; ++cc)
+                        *reinterpret_cast<uint4*>(S.c + row512(ent, cc)) = make_uint4(0, 0, 0, 0);
+            }
+            if (qa == 0) S.ok[ent] = kind != 0;
+        }
+        // the next chunk's rows, in flight during this chunk's MMAs and softmax
+        if (c + 1 < nchunks) load_row(ge2, pre_next);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // S^T = C Q^T (32 MMAs of K = 16 dims)
+        if (tid == 0 && ok) {
+            constexpr uint32_t id = idesc_f16(128, 64, 0, false, false);
+            for (int kk = 0; kk < kD / 16; ++kk)
+                mma_f16_ss(tmem + kQColS, umma_desc(sm_c + kk * 256, 128, 8192), umma_desc(sm_q + kk * 256, 128, 8192),
+                           id, kk > 0);
+            tc_commit(&S.bar);
+            pend = 1;
+        }
+        {
+            const bool w = __syncthreads_and(ok && mbar_wait(&S.bar, 0, wlim));
+            if (w) pend = 0;
+            ok = w;
+        }
+        tc_fence_after();
+
+        // softmax against the running maximum; P^T hi/lo into S.p
+        float alpha_l = 1.f;  // this lane's head hl: rescale factor of the accumulated O
+        if (ok) {
+            float x[32];
+            {
+                uint32_t r[32];
+                tmem_ld32(tmem + (uint32_t(32 * qd) << 16) + kQColS + 32 * hf, r);
+                tmem_ld_wait();
+                const bool oke = S.ok[e];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = oke ? sm_eff * __uint_as_float(r[j]) : -INFINITY;
+            }
+            auto reduce = [&](float(&v)[32], bool is_max) {  // lane l ends with head 32 hf + l
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const bool up = (lane & o) != 0;
+#pragma unroll
+                    for (int i = 0; i < o; ++i) {
+                        const float send = up ? v[i] : v[i + o];
+                        const float keep = up ? v[i + o] : v[i];
+                        const float got = __shfl_xor_sync(0xffffffffu, send, o);
+                        v[i] = is_max ? fmaxf(keep, got) : keep + got;
+                    }
+                }
+                return v[0];
+            };
+            {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = x[j];
+                red[qd][hl] = reduce(v, true);
+            }
+            __syncthreads();
+            const float m_old = S.m[hl];
+            const float mc = fmaxf(fmaxf(red[0][hl], red[1][hl]), fmaxf(red[2][hl], red[3][hl]));
+            const float m_new = fmaxf(m_old, mc);
+            alpha_l = m_old == -INFINITY ? 0.f : __expf(m_old - m_new);
+            float lh;
+            {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float m = __shfl_sync(0xffffffffu, m_new, j);
+                    x[j] = x[j] == -INFINITY ? 0.f : __expf(x[j] - m);
+                    v[j] = x[j];
+                }
+                lh = reduce(v, false);
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float a = x[8 * cc + 2 * t], b = x[8 * cc + 2 * t + 1];
+                    const __half2 h2 = __floats2half2_rn(a, b);
+                    const float2 hb = __half22float2(h2);
+                    const __half2 l2 = __floats2half2_rn(a - hb.x, b - hb.y);
+                    hi[t] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lo[t] = *reinterpret_cast<const uint32_t*>(&l2);
+                }
+                *reinterpret_cast<uint4*>(S.p + pmn(e, 32 * hf + 8 * cc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(S.p + pmn(e, 64 + 32 * hf + 8 * cc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            __syncthreads();  // every read of the maxima is done
+            red[qd][hl] = lh;
+            __syncthreads();
+            if (qd == 0) {
+                const float lc = red[0][hl] + red[1][hl] + red[2][hl] + red[3][hl];
+                S.l[hl] = S.l[hl] * alpha_l + lc;
+                S.m[hl] = m_new;
+                S.alpha[hl] = alpha_l;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // rescale the accumulated O where a head's maximum rose (uniform:
+        // every warp reads the same factors)
+        if (ok && c > 0) {
+            const bool any = __any_sync(0xffffffffu, S.alpha[lane] != 1.f || S.alpha[lane + 32] != 1.f);
+            if (any) {
+                for (int b2 = 0; b2 < 2; ++b2) {
+                    const int mb = 2 * (warp >> 2) + b2;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t ta = tmem + (uint32_t(32 * (warp & 3)) << 16) + kQColO + 64 * mb + 32 * half;
+                        uint32_t r[32];
+                        tmem_ld32(ta, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            r[j] = __float_as_uint(__uint_as_float(r[j]) * S.alpha[32 * half + j]);
+                        tmem_st32(ta, r);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+            }
+        }
+
+        // O^T += C^T P^T: per block of 128 dims, the hi part then the lo part
+        // into the same 64 columns
+        if (tid == 0 && ok) {
+            constexpr uint32_t id = idesc_f16(128, 64, 0, true, true);
+            for (int mb = 0; mb < 4; ++mb) {
+                const uint32_t d = tmem + kQColO + 64 * mb;
+                for (int part = 0; part < 2; ++part)
+                    for (int kk = 0; kk < kTcE / 16; ++kk)
+                        mma_f16_ss(d, umma_desc(sm_c + mb * 2048 + kk * 16384, 8192, 128),
+                                   umma_desc(pb + part * 1024 + kk * 4096, 2048, 128), id,
+                                   c > 0 || part > 0 || kk > 0);
+            }
+            tc_commit(&S.bar);
+            pend = 2;
+        }
+    }
+    {
+        const bool w = __syncthreads_and(ok && mbar_wait(&S.bar, 1, wlim));
+        if (w) pend = 0;
+        ok = w;
+    }
+    tc_fence_after();
+    if (ok) {  // O / l, rounded once; warp -> dims 32 (warp % 4) + lane of blocks 2 (warp / 4), +1
+        for (int b2 = 0; b2 < 2; ++b2) {
+            const int mb = 2 * (warp >> 2) + b2;
+            const int dim = mb * 128 + 32 * (warp & 3) + lane;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + kQColO + 64 * mb + 32 * half, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int h = 32 * half + j;
+                    const float L = S.l[h];
+                    const float o = L > 0.f ? __uint_as_float(r[j]) / L : 0.f;
+                    const int64_t oi = (q * kH + h) * int64_t(kD) + dim;
+                    if (out_f32)
+                        static_cast<float*>(out)[oi] = o;
+                    else
+                        static_cast<uint16_t*>(out)[oi] = bf16_bits(o);
+                }
+            }
+        }
+        if (out_lse && tid < kH) {
+            const float L = S.l[tid];
+            out_lse[q * kH + tid] = L > 0.f ? S.m[tid] + logf(L) : -INFINITY;
+        }
+    } else if (tid == 0) {
+        record(st, CSA2_ERR_TIMEOUT, 5, int32_t(q), 0);
+    }
+    if (tid == 0 && pend != 0) mbar_wait(&S.bar, pend - 1, kDrainNs);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kQCols);
+}
+
 // Opt both variants into their shared memory and note how many clusters of
 // `splits` CTAs can be resident at once (0 when clusters are unavailable).
 static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
@@ -631,7 +1015,9 @@ static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
         if (cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnTcSmem))) != cudaSuccess ||
             cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(sizeof(AttnTcSmem))) != cudaSuccess)
+                                 int(sizeof(AttnTcSmem))) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(AttnQSmem))) != cudaSuccess)
             return CSA2_ERR_CUDA;
         for (int c = 1; c <= 8; ++c) {
             cudaLaunchConfig_t cfg = {};
@@ -680,7 +1066,7 @@ static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* k
     if (!aligned16(q_bf16) || !aligned16(kv_codes) || !aligned16(out) || (swa && !aligned16(swa)))
         return CSA2_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(kv_scales) & 7) return CSA2_ERR_INVALID_ARG;
-    if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+    if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;  // grid.y of the split kernel (the per-query kernel uses grid.x)
     const AttnWs L = attn_ws(n_q, k, window);
     if (!ws || !aligned16(ws) || ws_bytes < L.total) return CSA2_ERR_WORKSPACE;
     if (n_q == 0) return CSA2_OK;
@@ -694,6 +1080,15 @@ static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* k
     int max_clusters = 0;
     csa2_status e = prepare_attn_tc(L.splits, &max_clusters);
     if (e != CSA2_OK) return e;
+    if (n_q >= kAttnQueryMin && k + window > 0) {
+        // many queries: one CTA per query over all its entries, no merge
+        timer_begin(K_ATTN_SPLIT, s);
+        const cudaError_t lq = launch(attn_query_kernel, dim3(unsigned(n_q)), kAttnThreads, sizeof(AttnQSmem), s, 1,
+                                      q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window,
+                                      win_shared, sm_scale, out, f32, out_lse, st, wait_limit_ns());
+        timer_end(K_ATTN_SPLIT, s);
+        return lq == cudaSuccess ? launch_status() : CSA2_ERR_CUDA;
+    }
     // one cluster per query when every cluster of the launch is resident at once
     const bool cluster = L.splits <= 8 && n_q <= max_clusters;
     const dim3 grid(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q), 1);
