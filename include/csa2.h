@@ -318,7 +318,7 @@ csa2_status csa2_sparse_attn_prefill(const void* q_bf16, int64_t n_q,
  * csa2_launch_count: kernels launched through the library by this process.
  * csa2_timer_enable: bracket the next max_launches launches of kernel
  *   `kernel_id` (0 scan_blockmax, 1 select_blocks, 2 pool_score,
- *   3 select_topk, 4 attn_split, 5 attn_merge, 6 quantize_fp4,
+ *   3 select_topk, 4 attn_split (either attention kernel), 5 attn_merge, 6 quantize_fp4,
  *   7 quantize_fp8, 8 rope_table) with CUDA events on their stream.  Not for
  *   use during stream capture.
  * csa2_timer_read: wait for those events, return the summed device time and
