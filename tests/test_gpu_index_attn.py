@@ -56,22 +56,26 @@ def test_many_query_shared_cache_m2():
         verify_query(g, wl, q, check_cache=(q == 0))
 
 
-def test_attention_direct_edge_cases():
+# reps 1: 4 queries (the split kernel, clusters of splits); reps 33: 132
+# queries (one CTA per query with an online softmax over 128-entry chunks)
+@pytest.mark.parametrize("reps", [1, 33])
+def test_attention_direct_edge_cases(reps):
     """Direct csa2_sparse_attn calls: -1 pads, empty selection, window 0,
-    single entry, and an out-of-range index that is skipped and recorded."""
+    single entry, and an out-of-range index that is skipped and recorded;
+    the bf16 output is the fp32 output rounded once."""
     from csa2_sparse_attention_gb300 import abi
     rng = np.random.default_rng(11)
-    n_rows, B, K, Wn = 64, 4, 8, 128
+    n_rows, B, K, Wn = 64, 4 * reps, 8, 128
     codes = rng.integers(0, 256, (n_rows, 256)).astype(np.uint8)
     scales = rng.integers(0x28, 0x38, (n_rows, 32)).astype(np.uint8)
     swa = rng.integers(0, 0x7E, (B, Wn, 512)).astype(np.uint8)
     q = torch.randn((B, 64, 512), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
-    kv_start = np.array([0, 16, 32, 48], dtype=np.int64)
-    n_vis = np.array([16, 1, 16, 12], dtype=np.int32)
+    kv_start = np.tile(np.array([0, 16, 32, 48], dtype=np.int64), reps)
+    n_vis = np.tile(np.array([16, 1, 16, 12], dtype=np.int32), reps)
     top = np.full((B, K), -1, dtype=np.int32)
-    top[0, :5] = [0, 3, 7, 8, 15]
-    top[1, 0] = 0
-    top[2, :3] = [1, 2, 99]          # 99 >= n: skipped and recorded
+    top[0::4, :5] = [0, 3, 7, 8, 15]
+    top[1::4, 0] = 0
+    top[2::4, :3] = [1, 2, 99]       # 99 >= n: skipped and recorded
     cases_window = 0
     d = "cuda"
     t = lambda a: torch.from_numpy(a).to(d)
@@ -83,7 +87,13 @@ def test_attention_direct_edge_cases():
                              t(swa), None, window, 1 / np.sqrt(512), out, abi.OUT_F32, lse, ws, ws.numel())
         torch.cuda.synchronize()
         st = abi.csa2_status_fetch(ws)
-        assert st[0] == abi.ERR_DEVICE_BOUNDS and st[1] == 7 and st[2] == 2 and st[3] == 99
+        assert st[0] == abi.ERR_DEVICE_BOUNDS and st[1] == 7 and st[2] % 4 == 2 and st[3] == 99
+        out16 = torch.zeros((B, 64, 512), dtype=torch.bfloat16, device=d)
+        ws16 = torch.zeros_like(ws)
+        abi.csa2_sparse_attn(q.to(d), B, t(codes), t(scales), n_rows, t(kv_start), t(n_vis), t(top), K,
+                             t(swa), None, window, 1 / np.sqrt(512), out16, abi.OUT_BF16, None, ws16, ws16.numel())
+        torch.cuda.synchronize()
+        assert torch.equal(out16, out.to(torch.bfloat16))
         qn = bf16_to_f64(q)
         for b in range(B):
             rows = codes[kv_start[b]:kv_start[b] + n_vis[b]]
@@ -128,23 +138,24 @@ def test_attention_bf16_output_within_its_rounding():
         assert np.all(err <= 2.0 ** -8 * np.abs(o_ref) + 1e-5 * np.abs(o_ref).max(axis=-1, keepdims=True))
 
 
-def test_attention_subnormal_window_bytes_and_scales():
+@pytest.mark.parametrize("reps", [1, 43])  # 3 queries (split kernel) or 129 (one CTA per query)
+def test_attention_subnormal_window_bytes_and_scales(reps):
     """Window bytes that are all E4M3 subnormals (|x| <= 7 * 2^-9) and FP4
     rows whose scales are all subnormal: the output is made of those values
     only, so a decode that flushed them to zero fails the relative check."""
     from csa2_sparse_attention_gb300 import abi
     rng = np.random.default_rng(12)
-    n_rows, B, K, Wn = 64, 3, 16, 128
+    n_rows, B, K, Wn = 64, 3 * reps, 16, 128
     codes = rng.integers(0, 256, (n_rows, 256)).astype(np.uint8)
     scales = rng.integers(0x01, 0x08, (n_rows, 32)).astype(np.uint8)          # subnormal scales
     sub = np.concatenate([np.arange(0x01, 0x08), np.arange(0x81, 0x88)]).astype(np.uint8)
     swa = rng.choice(sub, (B, Wn, 512)).astype(np.uint8)                     # subnormal window
     q = torch.randn((B, 64, 512), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
-    kv_start = np.array([0, 16, 32], dtype=np.int64)
-    n_vis = np.array([16, 16, 30], dtype=np.int32)
+    kv_start = np.tile(np.array([0, 16, 32], dtype=np.int64), reps)
+    n_vis = np.tile(np.array([16, 16, 30], dtype=np.int32), reps)
     top = np.full((B, K), -1, dtype=np.int32)
-    top[1, :6] = [0, 2, 4, 6, 8, 10]     # query 0: window only; 1: both; 2: top-k only (window 0)
-    top[2, :16] = np.arange(16)
+    top[1::3, :6] = [0, 2, 4, 6, 8, 10]  # query 0: window only; 1: both; 2: top-k only (window 0)
+    top[2::3, :16] = np.arange(16)
     d = "cuda"
     t = lambda a: torch.from_numpy(a).to(d)
     out = torch.zeros((B, 64, 512), dtype=torch.float32, device=d)
