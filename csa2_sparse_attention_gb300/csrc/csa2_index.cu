@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) score_tc_kernel(
     // shared memory are released
     int issued = 0, mma_n = 0;
     if (q_bf16 != nullptr && warp > 0) {
-        // the query as bf16: warps 1..5 quantize its 32 heads (256 groups of
+        // the query as bf16: warps 1..9 quantize its 32 heads (256 groups of
         // 16 channels) into the MMA's B operand and its scales, exactly as
         // the FP4 append does, while warp 0 already streams K tiles
         for (int grp = int(threadIdx.x) - 32; grp < 256; grp += kTcThreads - 32) {
@@ -303,8 +303,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) score_tc_kernel(
     }
 
     if (warp == 0) {  // ------------------------------------------ producer
-        // the scan copies a tile with two bulk copies from lane 0; the gather
-        // spreads a tile's 32 copies (16 blocks x codes, scales) over the lanes
+        // the scan copies a tile with one bulk copy from lane 0 (two in the
+        // split layout); the gather takes a tile's 16 blocks with four TMA
+        // gathers (records) or spreads 32 copies (codes, scales) over the lanes
         if (lane == 0 && q_bf16 == nullptr) {
             mbar_arrive_expect_tx(&S.qbar, 32 * 64);
             bulk_g2s(S.qcodes, q_codes + (q * 32 / 8) * 512, 32 * 64, &S.qbar);
