@@ -61,7 +61,7 @@ class LayerGroup:
     """Caches, per-layer inputs/outputs and workspaces of one workload."""
 
     def __init__(self, wl: W.Workload, device="cuda", sm_scale=1.0 / math.sqrt(512.0),
-                 rope_theta=10000.0, out_dtype=torch.float32, ik_layout=None, fused_q=True):
+                 rope_theta=10000.0, out_dtype=torch.float32, ik_layout=abi.LAYOUT_BLOCK8R, fused_q=True):
         self.wl = wl
         # fused_q: the index calls take the bf16 indexer query and quantize it
         # themselves (csa2_index_*_bf16); else a separate FP4 append per layer
@@ -92,8 +92,6 @@ class LayerGroup:
         self.kv_scales = torch.zeros((self.n_rows, 32), dtype=u8, device=d)
         # indexer K: 576-byte records of 8 rows (codes then scales), or BLOCK8
         # codes with a separate scale plane
-        if ik_layout is None:
-            ik_layout = abi.LAYOUT_BLOCK8R
         self.ik_layout = ik_layout
         if ik_layout == abi.LAYOUT_BLOCK8R:
             self.ik_codes = torch.zeros((self.n_rows // 8 * 576,), dtype=u8, device=d)
