@@ -62,11 +62,12 @@ struct AttnTcSmem {
 // canonical no-swizzle K-major offsets: rows of 512 16-bit elements, 16-byte
 // chunk c of row r -> (r/8)*8192 + c*128 + (r%8)*16
 __device__ __forceinline__ uint32_t row512(int r, int c) { return uint32_t((r >> 3) * 8192 + c * 128 + (r & 7) * 16); }
-// P^T [128 entries][128] f16, MN-major B operand of O^T: 8-entry groups of
-// 2 KB, 8-column chunks of 128 B; column n < 64 is head n's hi part, 64 + n
-// its lo part.
+// P^T [128 entries][NB] f16, MN-major B operand of O^T: 8-entry groups of
+// 16 NB bytes, 8-column chunks of 128 B; with NB = 2 x the CTA's heads,
+// column n < NB/2 is head n's hi part, NB/2 + n its lo part.
+template <int NB = 128>
 __device__ __forceinline__ uint32_t pmn(int e, int n) {
-    return uint32_t((e >> 3) * 2048 + (n >> 3) * 128 + (e & 7) * 16 + (n & 7) * 2);
+    return uint32_t((e >> 3) * (16 * NB) + (n >> 3) * 128 + (e & 7) * 16 + (n & 7) * 2);
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -140,13 +141,17 @@ __device__ __forceinline__ void fp8_quarter_to_c(const uint4* v, uint8_t* c, int
     }
 }
 
-// grid (splits, n_q), 256 threads, one CTA per SM.  The split's unnormalized
-// partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [64][512]) and (m_s, l_s) per
-// head go to the workspace, or (CLUSTER) are merged across the cluster.
+// grid (HG splits, n_q), 256 threads, one CTA per SM.  CTA x takes split
+// x % splits for the 64 / HG heads of head group x / splits.  The split's
+// unnormalized partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [heads][512])
+// and (m_s, l_s) per head go to the workspace, or (CLUSTER, one cluster per
+// head group of a query) are merged across the cluster.  With two head
+// groups each CTA takes in half of Q and exchanges half as many partial
+// bytes, for twice the CTAs: the launch form for small batches.
 // win_shared: the window rows come from swa [n_rows][512] at row kv_start +
 // position (a window over a sequence the queries share) instead of each
 // query's ring swa [n_q][window][512] at slot position mod window.
-template <bool CLUSTER>
+template <bool CLUSTER, int HG>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const uint16_t* __restrict__ qg, const uint8_t* __restrict__ kv_codes,
     const uint8_t* __restrict__ kv_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
@@ -154,10 +159,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, bool win_shared, float sm_scale,
     float* __restrict__ part_o, float* __restrict__ part_ml, int splits, void* __restrict__ out,
     bool out_f32, float* __restrict__ out_lse, Status* st, uint64_t wlim) {
+    static_assert(HG == 1 || (HG == 2 && CLUSTER), "head groups are merged inside their cluster");
+    constexpr int NH = kH / HG;  // heads of this CTA
+    constexpr int NB = 2 * NH;   // P^T columns: hi parts, then lo parts
+    constexpr int NJ = 16 / HG;  // 16-byte chunks of Q per thread
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     AttnTcSmem& S = *reinterpret_cast<AttnTcSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
-    const int split = blockIdx.x;
+    const int split = int(blockIdx.x) % splits, hg = int(blockIdx.x) / splits;
     const int64_t q = blockIdx.y;
 
     if (tid == 0) {
@@ -176,19 +185,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const int ge = ((ent >> 5) * splits + split) * 32 + (ent & 31);
     const int32_t pre = ge < k ? topk[q * k + ge] : -1;
     if (warp == 0) tmem_alloc(&S.tmem, kTcCols);
-    // Q chunk j of this thread (16 bytes): head 8 (g / 16) + lane % 8, chunk
-    // 4 (g % 16) + lane / 8 with g = 16 warp + j.  A quarter-warp covers 8
-    // heads (8 distinct bank groups in the canonical layout); an instruction
-    // reads 64 contiguous bytes of each of 8 rows.
+    // Q chunk j of this thread (16 bytes): head 8 (g / 16) + lane % 8 of the
+    // CTA's heads, chunk 4 (g % 16) + lane / 8 with g = NJ warp + j.  A
+    // quarter-warp covers 8 heads (8 distinct bank groups in the canonical
+    // layout); an instruction reads 64 contiguous bytes of each of 8 rows.
     auto q_chunk = [&](int j) {
-        const int g = 16 * warp + j;
+        const int g = NJ * warp + j;
         return (8 * (g >> 4) + (lane & 7)) * 64 + 4 * (g & 15) + (lane >> 3);
     };
-    uint4 qv[16];
+    uint4 qv[NJ];
     {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(qg + q * (kH * kD));
+        const uint4* qsrc = reinterpret_cast<const uint4*>(qg + q * (kH * kD) + hg * (NH * kD));
 #pragma unroll
-        for (int j = 0; j < 16; ++j) qv[j] = __ldg(qsrc + q_chunk(j));
+        for (int j = 0; j < NJ; ++j) qv[j] = __ldg(qsrc + q_chunk(j));
     }
     // the current token's bf16 window latent (two channels per thread), loaded
     // now by the split that holds its entry when the context fills the window
@@ -197,7 +206,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const uint32_t x_new = pre_new ? __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid) : 0u;
     int32_t n = 0;  // per-query validity, reported once per query
     {
-        const bool report = split == 0 && tid == 0;
+        const bool report = split == 0 && hg == 0 && tid == 0;
         if (ks < 0) {
             if (report) record(st, CSA2_ERR_DEVICE_BOUNDS, CHK_KV_START, int32_t(q), int32_t(ks));
         } else if (nv < 0 || ks + nv > n_rows) {
@@ -254,7 +263,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         uint8_t* ring = swa + (q * window + int64_t(n - 1) % window) * kD;
         const uint32_t x = pre_new ? x_new : __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid);
         const uint32_t b2 = e4m3x2_rn_sat(bf16_lo(x), bf16_hi(x));
-        reinterpret_cast<uint16_t*>(ring)[tid] = static_cast<uint16_t>(b2);
+        if (hg == 0) reinterpret_cast<uint16_t*>(ring)[tid] = static_cast<uint16_t>(b2);
         uint32_t h2[2];
         e4m3x4_to_f16x2(b2, h2);
         *reinterpret_cast<uint32_t*>(S.c + row512(cur_e, tid >> 2) + (tid & 3) * 4) = h2[0];
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     {
         uint32_t am = 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < NJ; ++j) {
             am = __vmaxu2(am, __vmaxu2(qv[j].x & 0x7FFF7FFFu, qv[j].y & 0x7FFF7FFFu));
             am = __vmaxu2(am, __vmaxu2(qv[j].z & 0x7FFF7FFFu, qv[j].w & 0x7FFF7FFFu));
         }
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         qs = qs < -126 ? -126 : (qs > 126 ? 126 : qs);
         const float qf = __uint_as_float(uint32_t(127 - qs) << 23);  // 2^-qs
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < NJ; ++j) {
             const int i = q_chunk(j);
             const uint32_t wv[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
             uint32_t o[4];
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 
     // S^T = C Q^T: 32 MMAs of K = 16 dims
     if (tid == 0) {
-        constexpr uint32_t id = idesc_f16(128, 64, 0, false, false);
+        constexpr uint32_t id = idesc_f16(128, NH, 0, false, false);
         for (int kk = 0; kk < kD / 16; ++kk)
             mma_f16_ss(tmem, umma_desc(sm_c + kk * 256, 128, 8192), umma_desc(sm_r0 + kk * 256, 128, 8192), id,
                        kk > 0);
@@ -334,14 +343,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     tc_fence_after();
 
     // softmax statistics from the registers: warp -> entries 32 (warp % 4) +
-    // lane, heads 32 (warp / 4) + j.  P^T (f16 hi for heads 0..63, lo for
-    // heads 64..127 of a 128-column B operand) goes to the consumed Q area.
+    // lane, heads 32 (warp / 4) + j of the CTA's (warps 4..7 idle with one
+    // group of 32 heads).  P^T (f16 hi parts in columns [0, NH), lo parts in
+    // [NH, NB) of the B operand) goes to the consumed Q area.
     uint8_t* pt = S.r0;
     float(*red)[kH] = reinterpret_cast<float(*)[kH]>(S.r0 + 32 * 1024);  // per lane quadrant, per head
     const int qd = warp & 3, hf = warp >> 2, e = 32 * qd + lane;
+    const bool sw = HG == 1 || hf < NH / 32;
     if (ok_mma) {
         float x[32];
-        {
+        if (sw) {
             uint32_t r[32];
             tmem_ld32(tmem + (uint32_t(32 * qd) << 16) + 32 * hf, r);
             tmem_ld_wait();
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             }
             return v[0];
         };
-        {
+        if (sw) {
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = x[j];
@@ -374,9 +385,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         }
         __syncthreads();
         const int hl = 32 * hf + lane;
-        const float mh = fmaxf(fmaxf(red[0][hl], red[1][hl]), fmaxf(red[2][hl], red[3][hl]));  // this split's max
-        float lh;
-        {
+        const float mh = sw ? fmaxf(fmaxf(red[0][hl], red[1][hl]), fmaxf(red[2][hl], red[3][hl])) : 0.f;
+        float lh = 0.f;
+        if (sw) {
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -387,7 +398,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             lh = reduce(v, false);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {  // P^T hi and lo, 8 heads per 16-byte store
+        for (int c = 0; c < 4 && sw; ++c) {  // P^T hi and lo, 8 heads per 16-byte store
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -398,13 +409,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
                 hi[t] = *reinterpret_cast<const uint32_t*>(&h2);
                 lo[t] = *reinterpret_cast<const uint32_t*>(&l2);
             }
-            *reinterpret_cast<uint4*>(pt + pmn(e, 32 * hf + 8 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(pt + pmn(e, 64 + 32 * hf + 8 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(pt + pmn<NB>(e, 32 * hf + 8 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(pt + pmn<NB>(e, NH + 32 * hf + 8 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         __syncthreads();  // every read of the maxima is done
-        red[qd][hl] = lh;
+        if (sw) red[qd][hl] = lh;
         __syncthreads();
-        if (qd == 0) {  // (m, l) of head hl
+        if (qd == 0 && sw) {  // (m, l) of head hl
             const float l = red[0][hl] + red[1][hl] + red[2][hl] + red[3][hl];
             if (CLUSTER) {
                 S.ml[hl][0] = mh;
@@ -422,17 +433,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     tc_fence_after();
 
     // O^T = C^T P^T: 4 blocks of 128 dims (C is the MN-major A operand), each
-    // into 128 TMEM columns: heads' hi parts, then their lo parts (an M = 128
+    // into NB TMEM columns: heads' hi parts, then their lo parts (an M = 128
     // MMA costs the same at N = 128 as at N = 64).  Block 0 overwrites S^T,
     // which has been read.
     if (tid == 0 && ok_mma) {
-        constexpr uint32_t id = idesc_f16(128, 128, 0, true, true);
+        constexpr uint32_t id = idesc_f16(128, NB, 0, true, true);
         const uint32_t pb = smem_addr(pt);
         for (int mb = 0; mb < 4; ++mb) {
-            const uint32_t d = tmem + 128 * mb;
+            const uint32_t d = tmem + NB * mb;
             for (int kk = 0; kk < kTcE / 16; ++kk)
-                mma_f16_ss(d, umma_desc(sm_c + mb * 2048 + kk * 16384, 8192, 128), umma_desc(pb + kk * 4096, 2048, 128),
-                           id, kk > 0);
+                mma_f16_ss(d, umma_desc(sm_c + mb * 2048 + kk * 16384, 8192, 128),
+                           umma_desc(pb + kk * (32 * NB), 16 * NB, 128), id, kk > 0);
         }
         tc_commit(&S.bar);
     }
@@ -449,10 +460,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             const int mb = 2 * (warp >> 2) + b2;
             const int dim = mb * 128 + 32 * (warp & 3) + lane;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            for (int half = 0; half < NH / 32; ++half) {
                 uint32_t rh[32], rl[32];
-                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + 128 * mb + 32 * half, rh);
-                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + 128 * mb + 64 + 32 * half, rl);
+                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + NB * mb + 32 * half, rh);
+                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + NB * mb + NH + 32 * half, rl);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
@@ -468,7 +479,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         cluster.sync();  // every partial and (m, l) of the query is visible
         const int rank = int(cluster.block_rank());
         float(*wts)[8] = reinterpret_cast<float(*)[8]>(S.r0);  // P is consumed: merge weights a_s / L
-        if (pending == 0 && tid < kH) {  // merge weights of head tid
+        if (pending == 0 && tid < NH) {  // merge weights of the CTA's head tid
             float mp[8], lp[8], M = -INFINITY;
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
@@ -490,7 +501,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
             for (int p = 0; p < 8; ++p) wts[tid][p] = a[p] * inv;
-            if (rank == 0 && out_lse) out_lse[q * kH + tid] = L > 0.f ? M + logf(L) : -INFINITY;
+            if (rank == 0 && out_lse) out_lse[q * kH + hg * NH + tid] = L > 0.f ? M + logf(L) : -INFINITY;
         }
         __syncthreads();
         // this CTA reduces dims [lo, hi) (whole float4s) over all peers
@@ -501,7 +512,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 #pragma unroll
         for (int p = 0; p < 8; ++p)
             px[p] = reinterpret_cast<const float4*>(cluster.map_shared_rank(X, p < splits ? p : 0));
-        for (int idx = tid; pending == 0 && idx < kH * w4; idx += kAttnThreads) {
+        for (int idx = tid; pending == 0 && idx < NH * w4; idx += kAttnThreads) {
             const int h = idx / w4, d4 = lo / 4 + idx % w4;
             float4 v[8];
 #pragma unroll
@@ -516,7 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
                 o.z = fmaf(wgt, v[p].z, o.z);
                 o.w = fmaf(wgt, v[p].w, o.w);
             }
-            const int64_t oi = (q * kH + h) * int64_t(kD) + 4 * d4;
+            const int64_t oi = (q * kH + hg * NH + h) * int64_t(kD) + 4 * d4;
             if (out_f32) {
                 *reinterpret_cast<float4*>(static_cast<float*>(out) + oi) = o;
             } else {
@@ -1012,9 +1023,11 @@ static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
     if (!done[dev]) {
-        if (cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attn_tc_kernel<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnTcSmem))) != cudaSuccess ||
-            cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(attn_tc_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(AttnTcSmem))) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_tc_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnTcSmem))) != cudaSuccess ||
             cudaFuncSetAttribute(attn_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnQSmem))) != cudaSuccess)
@@ -1032,7 +1045,7 @@ static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<true>, &cfg) != cudaSuccess) {
+            if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<true, 1>, &cfg) != cudaSuccess) {
                 n = 0;
                 cudaGetLastError();
             }
@@ -1089,17 +1102,23 @@ static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* k
         timer_end(K_ATTN_SPLIT, s);
         return lq == cudaSuccess ? launch_status() : CSA2_ERR_CUDA;
     }
-    // one cluster per query when every cluster of the launch is resident at once
+    // one cluster per query when every cluster of the launch is resident at
+    // once; two clusters per query (one per half of the heads) when those fit
+    // too, with at most one CTA per multiprocessor
     const bool cluster = L.splits <= 8 && n_q <= max_clusters;
-    const dim3 grid(static_cast<unsigned>(L.splits), static_cast<unsigned>(n_q), 1);
+    const bool halves = cluster && 2 * n_q <= max_clusters && 2 * n_q * L.splits <= sm_count();
+    const dim3 grid(static_cast<unsigned>(L.splits * (halves ? 2 : 1)), static_cast<unsigned>(n_q), 1);
     timer_begin(K_ATTN_SPLIT, s);
     const cudaError_t le =
-        cluster ? launch(attn_tc_kernel<true>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
-                         kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
-                         sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns())
-                : launch(attn_tc_kernel<false>, grid, kAttnThreads, sizeof(AttnTcSmem), s, 1, q, kv_codes,
-                         kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared, sm_scale,
-                         part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns());
+        halves    ? launch(attn_tc_kernel<true, 2>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
+                           kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
+                           sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns())
+        : cluster ? launch(attn_tc_kernel<true, 1>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
+                           kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
+                           sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns())
+                  : launch(attn_tc_kernel<false, 1>, grid, kAttnThreads, sizeof(AttnTcSmem), s, 1, q, kv_codes,
+                           kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared, sm_scale,
+                           part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns());
     timer_end(K_ATTN_SPLIT, s);
     if (le != cudaSuccess) return CSA2_ERR_CUDA;
     if (cluster) return launch_status();
