@@ -145,9 +145,9 @@ __device__ __forceinline__ void fp8_quarter_to_c(const uint4* v, uint8_t* c, int
 // x % splits for the 64 / HG heads of head group x / splits.  The split's
 // unnormalized partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [heads][512])
 // and (m_s, l_s) per head go to the workspace, or (CLUSTER, one cluster per
-// head group of a query) are merged across the cluster.  With two head
-// groups each CTA takes in half of Q and exchanges half as many partial
-// bytes, for twice the CTAs: the launch form for small batches.
+// head group of a query) are merged across the cluster.  With HG head
+// groups each CTA takes in 1/HG of Q and exchanges 1/HG of the partial
+// bytes, for HG times the CTAs: the launch form for small batches.
 // win_shared: the window rows come from swa [n_rows][512] at row kv_start +
 // position (a window over a sequence the queries share) instead of each
 // query's ring swa [n_q][window][512] at slot position mod window.
@@ -159,10 +159,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     uint8_t* __restrict__ swa, const uint16_t* __restrict__ swa_new, int window, bool win_shared, float sm_scale,
     float* __restrict__ part_o, float* __restrict__ part_ml, int splits, void* __restrict__ out,
     bool out_f32, float* __restrict__ out_lse, Status* st, uint64_t wlim) {
-    static_assert(HG == 1 || (HG == 2 && CLUSTER), "head groups are merged inside their cluster");
+    static_assert(HG == 1 || ((HG == 2 || HG == 4) && CLUSTER), "head groups are merged inside their cluster");
     constexpr int NH = kH / HG;  // heads of this CTA
     constexpr int NB = 2 * NH;   // P^T columns: hi parts, then lo parts
     constexpr int NJ = 16 / HG;  // 16-byte chunks of Q per thread
+    constexpr int NC = NH >= 32 ? 4 : NH / 8;  // 8-head chunks of a softmax warp
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     AttnTcSmem& S = *reinterpret_cast<AttnTcSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
@@ -343,13 +344,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     tc_fence_after();
 
     // softmax statistics from the registers: warp -> entries 32 (warp % 4) +
-    // lane, heads 32 (warp / 4) + j of the CTA's (warps 4..7 idle with one
-    // group of 32 heads).  P^T (f16 hi parts in columns [0, NH), lo parts in
+    // lane, heads 32 (warp / 4) + j of the CTA's (warps 4..7 idle with 32
+    // heads or fewer; with 16, columns 16..31 of the load are not S and are
+    // masked).  P^T (f16 hi parts in columns [0, NH), lo parts in
     // [NH, NB) of the B operand) goes to the consumed Q area.
     uint8_t* pt = S.r0;
     float(*red)[kH] = reinterpret_cast<float(*)[kH]>(S.r0 + 32 * 1024);  // per lane quadrant, per head
     const int qd = warp & 3, hf = warp >> 2, e = 32 * qd + lane;
-    const bool sw = HG == 1 || hf < NH / 32;
+    const bool sw = HG == 1 || hf < (NH + 31) / 32;
     if (ok_mma) {
         float x[32];
         if (sw) {
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             tmem_ld_wait();
             const bool oke = S.ok[e];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = oke ? sm_eff * __uint_as_float(r[j]) : -INFINITY;
+            for (int j = 0; j < 32; ++j) x[j] = (oke && j < NH) ? sm_eff * __uint_as_float(r[j]) : -INFINITY;
         }
         // transpose-reduce: in the round with offset o each lane keeps half
         // of its values and takes the partner's matching half, so lane l
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             lh = reduce(v, false);
         }
 #pragma unroll
-        for (int c = 0; c < 4 && sw; ++c) {  // P^T hi and lo, 8 heads per 16-byte store
+        for (int c = 0; c < NC && sw; ++c) {  // P^T hi and lo, 8 heads per 16-byte store
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -459,15 +461,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         for (int b2 = 0; b2 < 2; ++b2) {
             const int mb = 2 * (warp >> 2) + b2;
             const int dim = mb * 128 + 32 * (warp & 3) + lane;
+            if (NH >= 32) {
 #pragma unroll
-            for (int half = 0; half < NH / 32; ++half) {
-                uint32_t rh[32], rl[32];
-                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + NB * mb + 32 * half, rh);
-                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + NB * mb + NH + 32 * half, rl);
+                for (int half = 0; half < NH / 32; ++half) {
+                    uint32_t rh[32], rl[32];
+                    tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + NB * mb + 32 * half, rh);
+                    tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + NB * mb + NH + 32 * half, rl);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        X[(32 * half + j) * kD + dim] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+                }
+            } else {  // 16 heads: hi and lo parts in one 32-column load
+                uint32_t r[32];
+                tmem_ld32(tmem + (uint32_t(32 * (warp & 3)) << 16) + NB * mb, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    X[(32 * half + j) * kD + dim] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+                for (int j = 0; j < NH; ++j) X[j * kD + dim] = __uint_as_float(r[j]) + __uint_as_float(r[NH + j]);
             }
         }
     } else if (tid == 0) {
@@ -1029,6 +1039,8 @@ static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
                                  int(sizeof(AttnTcSmem))) != cudaSuccess ||
             cudaFuncSetAttribute(attn_tc_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnTcSmem))) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_tc_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(AttnTcSmem))) != cudaSuccess ||
             cudaFuncSetAttribute(attn_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnQSmem))) != cudaSuccess)
             return CSA2_ERR_CUDA;
@@ -1103,14 +1115,18 @@ static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* k
         return lq == cudaSuccess ? launch_status() : CSA2_ERR_CUDA;
     }
     // one cluster per query when every cluster of the launch is resident at
-    // once; two clusters per query (one per half of the heads) when those fit
-    // too, with at most one CTA per multiprocessor
+    // once; one cluster per half or quarter of the heads when those fit too,
+    // with at most one CTA per multiprocessor
     const bool cluster = L.splits <= 8 && n_q <= max_clusters;
-    const bool halves = cluster && 2 * n_q <= max_clusters && 2 * n_q * L.splits <= sm_count();
-    const dim3 grid(static_cast<unsigned>(L.splits * (halves ? 2 : 1)), static_cast<unsigned>(n_q), 1);
+    auto fits = [&](int hg) { return cluster && hg * n_q <= max_clusters && hg * n_q * L.splits <= sm_count(); };
+    const int hg = fits(4) ? 4 : fits(2) ? 2 : 1;
+    const dim3 grid(static_cast<unsigned>(L.splits * hg), static_cast<unsigned>(n_q), 1);
     timer_begin(K_ATTN_SPLIT, s);
     const cudaError_t le =
-        halves    ? launch(attn_tc_kernel<true, 2>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
+        hg == 4   ? launch(attn_tc_kernel<true, 4>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
+                           kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
+                           sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns())
+        : hg == 2 ? launch(attn_tc_kernel<true, 2>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
                            kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
                            sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns())
         : cluster ? launch(attn_tc_kernel<true, 1>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
