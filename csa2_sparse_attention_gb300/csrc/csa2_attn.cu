@@ -49,15 +49,21 @@ constexpr int kD = CSA2_LATENT_DIM;
 constexpr int kTcE = 128;          // entries per CTA = M of S^T
 constexpr uint32_t kTcCols = 512;  // TMEM columns: S^T [0, 64); then O^T, 4 blocks of 128 (the first over S^T)
 
-struct AttnTcSmem {
+template <int E>
+struct AttnTcSmemT {
     uint8_t r0[64 * 1024];         // Q f16 (B of S^T); then P^T hi/lo f16 [0, 32K) and softmax partials
-    uint8_t c[kTcE * 1024];        // C [128 entries][512] f16; then the fp32 partial (cluster merge)
-    int ok[kTcE];                  // entry valid
+    uint8_t c[E * 1024];           // C [E entries][512] f16; then the fp32 partial (cluster merge)
+    int ok[E];                     // entry valid
     uint32_t qmax[kAttnThreads / 32];  // per-warp max |Q| (bf16 magnitude bits)
     float ml[kH][2];               // this split's (m, l) per head
     uint64_t bar;                  // MMA completion (phase 0: S, phase 1: O)
     uint32_t tmem;
 };
+using AttnTcSmem = AttnTcSmemT<kTcE>;
+// 160 entries per CTA (two head groups of 32): 320 threads, two S^T tiles
+constexpr int kTcE2 = 160;
+constexpr int kAttnThreads2 = 320;
+static_assert(sizeof(AttnTcSmemT<kTcE2>) + 1024 <= 227 * 1024, "shared memory of the 160-entry form");
 
 // canonical no-swizzle K-major offsets: rows of 512 16-bit elements, 16-byte
 // chunk c of row r -> (r/8)*8192 + c*128 + (r%8)*16
@@ -147,12 +153,17 @@ __device__ __forceinline__ void fp8_quarter_to_c(const uint4* v, uint8_t* c, int
 // and (m_s, l_s) per head go to the workspace, or (CLUSTER, one cluster per
 // head group of a query) are merged across the cluster.  With HG head
 // groups each CTA takes in 1/HG of Q and exchanges 1/HG of the partial
-// bytes, for HG times the CTAs: the launch form for small batches.
+// bytes, for HG times the CTAs: the launch form for small batches.  With
+// E = 160 entries per CTA (two head groups, 320 threads) a query's 640
+// entries take 4 splits, so 16 queries fill 128 SMs in two head groups: C
+// is stored with entries 128 .. 159 first (rows 0 .. 31), then 0 .. 127, so
+// that S^T is two M = 128 tiles (storage rows 32 .. 159, and rows 0 .. 127
+// of which only the first 32 are kept) and O^T runs over the storage order.
 // win_shared: the window rows come from swa [n_rows][512] at row kv_start +
 // position (a window over a sequence the queries share) instead of each
 // query's ring swa [n_q][window][512] at slot position mod window.
-template <bool CLUSTER, int HG>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
+template <bool CLUSTER, int HG, int E = kTcE>
+__global__ void __launch_bounds__(E == kTcE ? kAttnThreads : kAttnThreads2, 1) attn_tc_kernel(
     const uint16_t* __restrict__ qg, const uint8_t* __restrict__ kv_codes,
     const uint8_t* __restrict__ kv_scales, int64_t n_rows, const int64_t* __restrict__ kv_start,
     const int32_t* __restrict__ n_visible, const int32_t* __restrict__ topk, int k,
@@ -164,8 +175,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     constexpr int NB = 2 * NH;   // P^T columns: hi parts, then lo parts
     constexpr int NJ = 16 / HG;  // 16-byte chunks of Q per thread
     constexpr int NC = NH >= 32 ? 4 : NH / 8;  // 8-head chunks of a softmax warp
+    static_assert(E == kTcE || (E == kTcE2 && HG == 2), "160 entries per CTA with two head groups only");
+    constexpr int T = E == kTcE ? kAttnThreads : kAttnThreads2;  // threads
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    AttnTcSmem& S = *reinterpret_cast<AttnTcSmem*>(smem_raw);
+    AttnTcSmemT<E>& S = *reinterpret_cast<AttnTcSmemT<E>*>(smem_raw);
     const int tid = threadIdx.x, lane = lane_id(), warp = tid >> 5;
     const int split = int(blockIdx.x) % splits, hg = int(blockIdx.x) / splits;
     const int64_t q = blockIdx.y;
@@ -182,7 +195,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     // the sequence (top-k entries, then window entries) in groups of 32:
     // split s takes groups s, s + splits, s + 2 splits, s + 3 splits, so the
     // splits get about the same mix and each warp one kind of entry
-    const int ent = tid & (kTcE - 1), qa = tid >> 7;  // entry; channel quarters qa, qa + 2
+    const int ent = tid % E, qa = tid / E;  // entry; channel quarters qa, qa + 2
+    // C row of entry e: itself, or (160 entries) 128 .. 159 first
+    auto srow = [](int e) { return E == kTcE ? e : (e < kTcE ? e + (E - kTcE) : e - kTcE); };
     const int ge = ((ent >> 5) * splits + split) * 32 + (ent & 31);
     const int32_t pre = ge < k ? topk[q * k + ge] : -1;
     if (warp == 0) tmem_alloc(&S.tmem, kTcCols);
@@ -194,8 +209,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         const int g = NJ * warp + j;
         return (8 * (g >> 4) + (lane & 7)) * 64 + 4 * (g & 15) + (lane >> 3);
     };
+    const bool qw = T == kAttnThreads || warp < kAttnThreads / 32;  // warps that carry Q
     uint4 qv[NJ];
-    {
+    if (qw) {
         const uint4* qsrc = reinterpret_cast<const uint4*>(qg + q * (kH * kD) + hg * (NH * kD));
 #pragma unroll
         for (int j = 0; j < NJ; ++j) qv[j] = __ldg(qsrc + q_chunk(j));
@@ -204,7 +220,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     // now by the split that holds its entry when the context fills the window
     // (the usual case), so it does not wait for the context length
     const bool pre_new = swa_new != nullptr && window > 0 && ((k + window - 1) >> 5) % splits == split;
-    const uint32_t x_new = pre_new ? __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid) : 0u;
+    const uint32_t x_new =
+        pre_new && tid < kD / 2 ? __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid) : 0u;
     int32_t n = 0;  // per-query validity, reported once per query
     {
         const bool report = split == 0 && hg == 0 && tid == 0;
@@ -260,14 +277,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             }
         }
     }
-    if (cur_e >= 0) {  // E4M3 of the current token's bf16 latent, two channels per thread: to the ring and into C
+    if (cur_e >= 0 && tid < kD / 2) {  // E4M3 of the current token's bf16 latent, two channels per thread: ring and C
         uint8_t* ring = swa + (q * window + int64_t(n - 1) % window) * kD;
         const uint32_t x = pre_new ? x_new : __ldg(reinterpret_cast<const uint32_t*>(swa_new + q * kD) + tid);
         const uint32_t b2 = e4m3x2_rn_sat(bf16_lo(x), bf16_hi(x));
         if (hg == 0) reinterpret_cast<uint16_t*>(ring)[tid] = static_cast<uint16_t>(b2);
         uint32_t h2[2];
         e4m3x4_to_f16x2(b2, h2);
-        *reinterpret_cast<uint32_t*>(S.c + row512(cur_e, tid >> 2) + (tid & 3) * 4) = h2[0];
+        *reinterpret_cast<uint32_t*>(S.c + row512(srow(cur_e), tid >> 2) + (tid & 3) * 4) = h2[0];
     }
     // Q is stored as f16 times 2^-qs, qs chosen so that max|Q| 2^-qs lies in
     // [2^14, 2^15): exact for every element above max|Q| 2^-28, the rest within
@@ -275,12 +292,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     {
         uint32_t am = 0;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
+        for (int j = 0; j < NJ && qw; ++j) {
             am = __vmaxu2(am, __vmaxu2(qv[j].x & 0x7FFF7FFFu, qv[j].y & 0x7FFF7FFFu));
             am = __vmaxu2(am, __vmaxu2(qv[j].z & 0x7FFF7FFFu, qv[j].w & 0x7FFF7FFFu));
         }
         am = __reduce_max_sync(0xffffffffu, max(am & 0xFFFFu, am >> 16));
-        if (lane == 0) S.qmax[warp] = am;
+        if (lane == 0 && qw) S.qmax[warp] = am;
     }
     __syncthreads();  // max |Q| per warp, the current token's row, the barrier
     int qs = 0;
@@ -292,7 +309,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         qs = qs < -126 ? -126 : (qs > 126 ? 126 : qs);
         const float qf = __uint_as_float(uint32_t(127 - qs) << 23);  // 2^-qs
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
+        for (int j = 0; j < NJ && qw; ++j) {
             const int i = q_chunk(j);
             const uint32_t wv[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
             uint32_t o[4];
@@ -306,17 +323,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         }
     }
     // dequantize this thread's row into C
+    const int er = srow(ent);
     if (kind == 1) {
-        fp4_quarter_to_c(rv, rs0, S.c, ent, qa);
-        fp4_quarter_to_c(rv + 4, rs1, S.c, ent, qa + 2);
+        fp4_quarter_to_c(rv, rs0, S.c, er, qa);
+        fp4_quarter_to_c(rv + 4, rs1, S.c, er, qa + 2);
     } else if (kind == 2) {
-        fp8_quarter_to_c(rv, S.c, ent, qa);
-        fp8_quarter_to_c(rv + 8, S.c, ent, qa + 2);
+        fp8_quarter_to_c(rv, S.c, er, qa);
+        fp8_quarter_to_c(rv + 8, S.c, er, qa + 2);
     } else if (kind == 0) {
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2)
             for (int c = (qa + 2 * h2) * 16; c < (qa + 2 * h2) * 16 + 16; ++c)
-                *reinterpret_cast<uint4*>(S.c + row512(ent, c)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(S.c + row512(er, c)) = make_uint4(0, 0, 0, 0);
     }
     if (qa == 0) S.ok[ent] = kind != 0;
     const float sm_eff = sm_scale * __uint_as_float(uint32_t(127 + qs) << 23);  // logits scale of the f16 S
@@ -327,12 +345,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     const uint32_t tmem = S.tmem;
     const uint32_t sm_c = smem_addr(S.c), sm_r0 = smem_addr(S.r0);
 
-    // S^T = C Q^T: 32 MMAs of K = 16 dims
+    // S^T = C Q^T: 32 MMAs of K = 16 dims per 128-entry tile (160 entries:
+    // storage rows 32 .. 159 into columns [0, NH), rows 0 .. 127 into
+    // [NH, 2 NH), whose first 32 rows are entries 128 .. 159)
     if (tid == 0) {
         constexpr uint32_t id = idesc_f16(128, NH, 0, false, false);
-        for (int kk = 0; kk < kD / 16; ++kk)
-            mma_f16_ss(tmem, umma_desc(sm_c + kk * 256, 128, 8192), umma_desc(sm_r0 + kk * 256, 128, 8192), id,
-                       kk > 0);
+#pragma unroll 1
+        for (int t = 0; t < (E == kTcE ? 1 : 2); ++t) {
+            const uint32_t a0 = sm_c + (E == kTcE || t == 1 ? 0u : uint32_t(E - kTcE) / 8 * 8192);
+            for (int kk = 0; kk < kD / 16; ++kk)
+                mma_f16_ss(tmem + NH * t, umma_desc(a0 + kk * 256, 128, 8192), umma_desc(sm_r0 + kk * 256, 128, 8192),
+                           id, kk > 0);
+        }
         tc_commit(&S.bar);
     }
     // ok_mma: the MMAs issued so far are done.  A wait that gives up leaves
@@ -348,15 +372,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     // heads or fewer; with 16, columns 16..31 of the load are not S and are
     // masked).  P^T (f16 hi parts in columns [0, NH), lo parts in
     // [NH, NB) of the B operand) goes to the consumed Q area.
+    // With 160 entries warps 0..3 take entries 32 warp + lane (tile 0) and
+    // warp 4 entries 128 + lane (tile 1, lanes 0..31).
     uint8_t* pt = S.r0;
-    float(*red)[kH] = reinterpret_cast<float(*)[kH]>(S.r0 + 32 * 1024);  // per lane quadrant, per head
-    const int qd = warp & 3, hf = warp >> 2, e = 32 * qd + lane;
-    const bool sw = HG == 1 || hf < (NH + 31) / 32;
+    float(*red)[kH] = reinterpret_cast<float(*)[kH]>(S.r0 + 32 * 1024);  // per entry row block, per head
+    constexpr int NR = E / 32 > 4 ? E / 32 : 4;  // entry row blocks
+    const int qd = warp & 3, hf = E == kTcE ? warp >> 2 : 0;
+    const int rb = E == kTcE ? qd : warp;  // this warp's row block
+    const int e = 32 * rb + lane;
+    const bool sw = E == kTcE ? (HG == 1 || hf < (NH + 31) / 32) : warp < NR;
     if (ok_mma) {
         float x[32];
         if (sw) {
             uint32_t r[32];
-            tmem_ld32(tmem + (uint32_t(32 * qd) << 16) + 32 * hf, r);
+            tmem_ld32(tmem + (uint32_t(32 * qd) << 16) + 32 * hf + (rb >= 4 ? NH : 0), r);
             tmem_ld_wait();
             const bool oke = S.ok[e];
 #pragma unroll
@@ -383,11 +412,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = x[j];
-            red[qd][32 * hf + lane] = reduce(v, true);
+            red[rb][32 * hf + lane] = reduce(v, true);
         }
         __syncthreads();
         const int hl = 32 * hf + lane;
-        const float mh = sw ? fmaxf(fmaxf(red[0][hl], red[1][hl]), fmaxf(red[2][hl], red[3][hl])) : 0.f;
+        float mh = 0.f;
+        if (sw) {
+            mh = red[0][hl];
+#pragma unroll
+            for (int b = 1; b < NR; ++b) mh = fmaxf(mh, red[b][hl]);  // this split's max
+        }
         float lh = 0.f;
         if (sw) {
             float v[32];
@@ -411,14 +445,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
                 hi[t] = *reinterpret_cast<const uint32_t*>(&h2);
                 lo[t] = *reinterpret_cast<const uint32_t*>(&l2);
             }
-            *reinterpret_cast<uint4*>(pt + pmn<NB>(e, 32 * hf + 8 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(pt + pmn<NB>(e, NH + 32 * hf + 8 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(pt + pmn<NB>(srow(e), 32 * hf + 8 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(pt + pmn<NB>(srow(e), NH + 32 * hf + 8 * c)) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         __syncthreads();  // every read of the maxima is done
-        if (sw) red[qd][hl] = lh;
+        if (sw) red[rb][hl] = lh;
         __syncthreads();
-        if (qd == 0 && sw) {  // (m, l) of head hl
-            const float l = red[0][hl] + red[1][hl] + red[2][hl] + red[3][hl];
+        if (rb == 0 && sw) {  // (m, l) of head hl
+            float l = red[0][hl] + red[1][hl] + red[2][hl] + red[3][hl];
+#pragma unroll
+            for (int b = 4; b < NR; ++b) l += red[b][hl];
             if (CLUSTER) {
                 S.ml[hl][0] = mh;
                 S.ml[hl][1] = l;
@@ -443,7 +480,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
         const uint32_t pb = smem_addr(pt);
         for (int mb = 0; mb < 4; ++mb) {
             const uint32_t d = tmem + NB * mb;
-            for (int kk = 0; kk < kTcE / 16; ++kk)
+            for (int kk = 0; kk < E / 16; ++kk)
                 mma_f16_ss(d, umma_desc(sm_c + mb * 2048 + kk * 16384, 8192, 128),
                            umma_desc(pb + kk * (32 * NB), 16 * NB, 128), id, kk > 0);
         }
@@ -457,7 +494,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
     // warp -> dims 32*(warp%4) + lane of blocks 2*(warp/4), +1: to the
     // workspace, or (CLUSTER) to this CTA's shared memory (C is consumed)
     float* X = CLUSTER ? reinterpret_cast<float*>(S.c) : part_o + (q * splits + split) * int64_t(kH * kD);
-    if (ok_mma) {
+    if (ok_mma && warp < 8) {
         for (int b2 = 0; b2 < 2; ++b2) {
             const int mb = 2 * (warp >> 2) + b2;
             const int dim = mb * 128 + 32 * (warp & 3) + lane;
@@ -522,7 +559,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(
 #pragma unroll
         for (int p = 0; p < 8; ++p)
             px[p] = reinterpret_cast<const float4*>(cluster.map_shared_rank(X, p < splits ? p : 0));
-        for (int idx = tid; pending == 0 && idx < NH * w4; idx += kAttnThreads) {
+        for (int idx = tid; pending == 0 && idx < NH * w4; idx += T) {
             const int h = idx / w4, d4 = lo / 4 + idx % w4;
             float4 v[8];
 #pragma unroll
@@ -1025,11 +1062,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_query_kernel(
     if (warp == 0) tmem_dealloc(tmem, kQCols);
 }
 
-// Opt both variants into their shared memory and note how many clusters of
-// `splits` CTAs can be resident at once (0 when clusters are unavailable).
-static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
+// Opt the variants into their shared memory and note how many clusters of
+// `splits` CTAs can be resident at once (0 when clusters are unavailable),
+// for 128 entries per CTA and (max_clusters2) for 160.
+static int max_active_clusters(void (*kernel)(const uint16_t*, const uint8_t*, const uint8_t*, int64_t,
+                                              const int64_t*, const int32_t*, const int32_t*, int, uint8_t*,
+                                              const uint16_t*, int, bool, float, float*, float*, int, void*, bool,
+                                              float*, Status*, uint64_t),
+                               int threads, size_t smem, int c) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(c), 1, 1);
+    cfg.blockDim = dim3(unsigned(threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(c);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        n = 0;
+        cudaGetLastError();
+    }
+    return n;
+}
+
+static csa2_status prepare_attn_tc(int splits, int splits2, int* max_clusters, int* max_clusters2) {
     static bool done[64] = {};
-    static int cached[64][9] = {};
+    static int cached[64][9] = {}, cached2[64][9] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
     if (!done[dev]) {
@@ -1041,31 +1103,20 @@ static csa2_status prepare_attn_tc(int splits, int* max_clusters) {
                                  int(sizeof(AttnTcSmem))) != cudaSuccess ||
             cudaFuncSetAttribute(attn_tc_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnTcSmem))) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_tc_kernel<true, 2, kTcE2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(AttnTcSmemT<kTcE2>))) != cudaSuccess ||
             cudaFuncSetAttribute(attn_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(sizeof(AttnQSmem))) != cudaSuccess)
             return CSA2_ERR_CUDA;
         for (int c = 1; c <= 8; ++c) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(unsigned(c), 1, 1);
-            cfg.blockDim = dim3(kAttnThreads, 1, 1);
-            cfg.dynamicSmemBytes = sizeof(AttnTcSmem);
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = unsigned(c);
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<true, 1>, &cfg) != cudaSuccess) {
-                n = 0;
-                cudaGetLastError();
-            }
-            cached[dev][c] = n;
+            cached[dev][c] = max_active_clusters(attn_tc_kernel<true, 1>, kAttnThreads, sizeof(AttnTcSmem), c);
+            cached2[dev][c] =
+                max_active_clusters(attn_tc_kernel<true, 2, kTcE2>, kAttnThreads2, sizeof(AttnTcSmemT<kTcE2>), c);
         }
         done[dev] = true;
     }
     *max_clusters = (splits >= 1 && splits <= 8) ? cached[dev][splits] : 0;
+    *max_clusters2 = (splits2 >= 1 && splits2 <= 8) ? cached2[dev][splits2] : 0;
     return CSA2_OK;
 }
 
@@ -1102,8 +1153,9 @@ static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* k
     const uint16_t* q = static_cast<const uint16_t*>(q_bf16);
     const uint16_t* sn = static_cast<const uint16_t*>(swa_new_bf16);
     const bool f32 = out_dtype == CSA2_OUT_F32;
-    int max_clusters = 0;
-    csa2_status e = prepare_attn_tc(L.splits, &max_clusters);
+    int max_clusters = 0, max_clusters2 = 0;
+    const int splits2 = (k + window + kTcE2 - 1) / kTcE2;  // splits of 160 entries
+    csa2_status e = prepare_attn_tc(L.splits, splits2, &max_clusters, &max_clusters2);
     if (e != CSA2_OK) return e;
     if (n_q >= kAttnQueryMin && k + window > 0) {
         // many queries: one CTA per query over all its entries, no merge
@@ -1116,14 +1168,21 @@ static csa2_status sparse_attn(const void* q_bf16, int64_t n_q, const uint8_t* k
     }
     // one cluster per query when every cluster of the launch is resident at
     // once; one cluster per half or quarter of the heads when those fit too,
-    // with at most one CTA per multiprocessor
+    // with at most one CTA per multiprocessor; else halves of the heads over
+    // fewer splits of 160 entries
     const bool cluster = L.splits <= 8 && n_q <= max_clusters;
     auto fits = [&](int hg) { return cluster && hg * n_q <= max_clusters && hg * n_q * L.splits <= sm_count(); };
     const int hg = fits(4) ? 4 : fits(2) ? 2 : 1;
-    const dim3 grid(static_cast<unsigned>(L.splits * hg), static_cast<unsigned>(n_q), 1);
+    const bool e160 = hg == 1 && cluster && splits2 < L.splits && splits2 <= 8 && 2 * n_q <= max_clusters2 &&
+                      2 * n_q * splits2 <= sm_count();
+    const dim3 grid(static_cast<unsigned>(e160 ? 2 * splits2 : L.splits * hg), static_cast<unsigned>(n_q), 1);
     timer_begin(K_ATTN_SPLIT, s);
     const cudaError_t le =
-        hg == 4   ? launch(attn_tc_kernel<true, 4>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
+        e160      ? launch(attn_tc_kernel<true, 2, kTcE2>, grid, kAttnThreads2, sizeof(AttnTcSmemT<kTcE2>), s,
+                           unsigned(splits2), q, kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn,
+                           window, win_shared, sm_scale, part_o, part_ml, splits2, out, f32, out_lse, st,
+                           wait_limit_ns())
+        : hg == 4 ? launch(attn_tc_kernel<true, 4>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
                            kv_codes, kv_scales, n_rows, kv_start, n_visible, topk, k, swa, sn, window, win_shared,
                            sm_scale, part_o, part_ml, L.splits, out, f32, out_lse, st, wait_limit_ns())
         : hg == 2 ? launch(attn_tc_kernel<true, 2>, grid, kAttnThreads, sizeof(AttnTcSmem), s, unsigned(L.splits), q,
