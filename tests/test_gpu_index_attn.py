@@ -56,9 +56,12 @@ def test_many_query_shared_cache_m2():
         verify_query(g, wl, q, check_cache=(q == 0))
 
 
-# reps 1: 4 queries (the split kernel, clusters of splits); reps 33: 132
-# queries (one CTA per query with an online softmax over 128-entry chunks)
-@pytest.mark.parametrize("reps", [1, 33])
+# The batch size picks the attention launch form (8 + 128 entries per query,
+# so 2 splits of 128 or 1 of 160).  On a 152-SM GB300: reps 1 (4 queries)
+# four head groups per query, reps 5 (20) two head groups, reps 10 (40) two
+# head groups over one 160-entry split, reps 33 (132) one CTA per query with
+# an online softmax over 128-entry chunks.
+@pytest.mark.parametrize("reps", [1, 5, 10, 33])
 def test_attention_direct_edge_cases(reps):
     """Direct csa2_sparse_attn calls: -1 pads, empty selection, window 0,
     single entry, and an out-of-range index that is skipped and recorded;
@@ -138,7 +141,9 @@ def test_attention_bf16_output_within_its_rounding():
         assert np.all(err <= 2.0 ** -8 * np.abs(o_ref) + 1e-5 * np.abs(o_ref).max(axis=-1, keepdims=True))
 
 
-@pytest.mark.parametrize("reps", [1, 43])  # 3 queries (split kernel) or 129 (one CTA per query)
+# 3 queries (four head groups), 42 (two head groups over one 160-entry split)
+# or 129 (one CTA per query)
+@pytest.mark.parametrize("reps", [1, 14, 43])
 def test_attention_subnormal_window_bytes_and_scales(reps):
     """Window bytes that are all E4M3 subnormals (|x| <= 7 * 2^-9) and FP4
     rows whose scales are all subnormal: the output is made of those values
