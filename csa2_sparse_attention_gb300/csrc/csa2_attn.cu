@@ -27,6 +27,10 @@
 // reduces one slice of the dims over its peers through distributed shared
 // memory.  Otherwise the partials go to the workspace and a merge kernel
 // combines them.  Either way the result is rounded once, to fp32 or bf16.
+// Small batches spread the 64 heads over two or four clusters per query
+// (each CTA then takes in a part of Q and exchanges a part of the partial),
+// and somewhat larger batches (16-19 queries of 640 entries) take two head
+// groups over splits of 160 entries, so that the CTAs still fit one per SM.
 //
 // Optionally the kernel also appends the current token's window latent: the
 // bf16 row for position n-1 is rounded to E4M3 (as csa2_quantize_append FP8
@@ -147,7 +151,7 @@ __device__ __forceinline__ void fp8_quarter_to_c(const uint4* v, uint8_t* c, int
     }
 }
 
-// grid (HG splits, n_q), 256 threads, one CTA per SM.  CTA x takes split
+// grid (HG splits, n_q), 256 threads (320 with E = 160), one CTA per SM.  CTA x takes split
 // x % splits for the 64 / HG heads of head group x / splits.  The split's
 // unnormalized partial O_s = sum_j exp(l_j - m_s) c_j (fp32 [heads][512])
 // and (m_s, l_s) per head go to the workspace, or (CLUSTER, one cluster per
@@ -193,8 +197,8 @@ __global__ void __launch_bounds__(E == kTcE ? kAttnThreads : kAttnThreads2, 1) a
     const int64_t ks = kv_start[q];
     const int32_t nv = n_visible[q];
     // the sequence (top-k entries, then window entries) in groups of 32:
-    // split s takes groups s, s + splits, s + 2 splits, s + 3 splits, so the
-    // splits get about the same mix and each warp one kind of entry
+    // split s takes groups s, s + splits, s + 2 splits, ... (E / 32 of them),
+    // so the splits get about the same mix and each warp one kind of entry
     const int ent = tid % E, qa = tid / E;  // entry; channel quarters qa, qa + 2
     // C row of entry e: itself, or (160 entries) 128 .. 159 first
     auto srow = [](int e) { return E == kTcE ? e : (e < kTcE ? e + (E - kTcE) : e - kTcE); };
