@@ -1069,11 +1069,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_query_kernel(
 // Opt the variants into their shared memory and note how many clusters of
 // `splits` CTAs can be resident at once (0 when clusters are unavailable),
 // for 128 entries per CTA and (max_clusters2) for 160.
-static int max_active_clusters(void (*kernel)(const uint16_t*, const uint8_t*, const uint8_t*, int64_t,
-                                              const int64_t*, const int32_t*, const int32_t*, int, uint8_t*,
-                                              const uint16_t*, int, bool, float, float*, float*, int, void*, bool,
-                                              float*, Status*, uint64_t),
-                               int threads, size_t smem, int c) {
+template <class Kernel>
+static int max_active_clusters(Kernel kernel, int threads, size_t smem, int c) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(c), 1, 1);
     cfg.blockDim = dim3(unsigned(threads), 1, 1);
